@@ -1,0 +1,452 @@
+/*
+ * CPU oracle for the WNA16 routed-expert MoE forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may load this library.  The CUDA
+ * product path never calls, links or includes anything from this directory,
+ * and this file shares no code, header, table or helper with that path.
+ *
+ * What it computes, step by step, in the plainest order (no tiling, no fusion):
+ *
+ *   1. unpack   INT32 words -> signed codes           (format: "compressed-tensors
+ *               WNA16 format with FP16 group scales and INT32 packed values",
+ *               hampsonw/DeepSeek-V4-Flash-0731-WNA16, section "What changed";
+ *               "packed the signed codes with compressed-tensors",
+ *               section "How it was created", step 4)
+ *   2. dequant  W[n][k] = bf16_rne(code * scale[n][k / group])  (symmetric, no
+ *               zero point, one FP16 scale per group of input-dim weights;
+ *               same page, "What changed": "symmetric W2A16 quantization with
+ *               group size 128")
+ *   3. gather   each routed slot f = t*topk + j uses expert ids[t][j]
+ *               ("indexed MoE", Incubate DeepSeek V4 WNA16 runtime on SM86,
+ *               section "What this branch adds", item 3)
+ *   4. w13      g = W1 x, u = W3 x with W1 = rows [0, N) and W3 = rows [N, 2N)
+ *               of the fused gate/up tensor (same section, item 2)
+ *   5. SwiGLU   h = bf16_rne( silu(min(g, L)) * clamp(u, -L, L) )  (same
+ *               section, item 9: "SwiGLU alpha, beta, and clamp semantics";
+ *               alpha = 1, beta = 0, L = swiglu_limit)
+ *   6. w2       y = bf16_rne( W2 h )
+ *   7. combine  out[t] = bf16_rne( sum_j  w[t][j] * y[t*topk + j] ), j ascending
+ *
+ * Readings of points the pages leave open (each is listed in the design doc):
+ *   - in-word order: field j of a word holds element p*word + j at bits
+ *     [b*j, b*j + b), least significant first;
+ *   - stored field = code + 2^(b-1) (2-bit: code + 2, 4-bit: code + 8);
+ *   - the group axis is the reduction (input) dim of each projection;
+ *   - dequantised weights, h and y are rounded to BF16 (the operands the
+ *     BF16 tensor cores consume); accumulation is exact-ish (fp64 by default,
+ *     fp32 in the optional mode), each dot product in ascending k;
+ *   - routing weights are applied in the combine, in fp32/fp64, j ascending.
+ *
+ * The only source of randomness is the inputs; nothing here draws numbers.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ */
+/* Planted mistakes, used only by the pin tests to show that each pin   */
+/* catches a plausible bug.  0 = the correct oracle.                     */
+/* ------------------------------------------------------------------ */
+enum {
+    MUT_NONE = 0,
+    MUT_MSB_FIRST = 1,      /* unpack fields most-significant first            */
+    MUT_CODE_OFFSET = 2,    /* subtract 2^(b-1) - 1 instead of 2^(b-1)          */
+    MUT_GATE_UP_SWAP = 3,   /* use rows [N,2N) as gate and [0,N) as up          */
+    MUT_NO_CLAMP = 4,       /* drop the SwiGLU clamp                            */
+    MUT_GROUP_AXIS = 5,     /* index scales with (k % groups) instead of k/g    */
+    MUT_W2_TRANSPOSE = 6,   /* read w2 as [N, K] instead of [K, N]              */
+    MUT_NO_ROUTE_WEIGHT = 7,/* drop the routing weight in the combine           */
+    MUT_UNSTABLE_PERM = 8,  /* emit each expert's slots in descending order     */
+    MUT_SILU_SIGN = 9,      /* silu(z) = z / (1 + exp(z))                        */
+    MUT_LAST = 10
+};
+static int g_mutation = MUT_NONE;
+
+int oracle_set_mutation(int m)
+{
+    if (m < 0 || m >= MUT_LAST) return -1;
+    g_mutation = m;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Number formats (written from the IEEE-754 definitions).               */
+/* ------------------------------------------------------------------ */
+
+/* IEEE binary16 -> double, exact. */
+double oracle_fp16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int exp = (h >> 10) & 0x1f;
+    int man = h & 0x3ff;
+    double v;
+    if (exp == 0)
+        v = ldexp((double)man, -24);                 /* subnormal or zero */
+    else if (exp == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexp((double)(man | 0x400), exp - 25);  /* 1.man * 2^(exp-15) */
+    return sign ? -v : v;
+}
+
+/* bfloat16 -> double, exact (bf16 is the top half of a binary32). */
+double oracle_bf16_to_double(uint16_t b)
+{
+    uint32_t bits = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* Round a real value (given as a double) to the nearest bfloat16, ties to
+ * even, in ONE rounding step.  bfloat16 has 8 significant bits and the
+ * binary32 exponent range (normal exponents -126..127, subnormals down to
+ * 2^-133).  Overflow goes to infinity. */
+uint16_t oracle_bf16_rne(double v)
+{
+    uint32_t bits;
+    float f;
+    if (isnan(v)) return 0x7fc0;
+    if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+    int neg = v < 0;
+    double a = neg ? -v : v;
+    if (isinf(a)) return neg ? 0xff80 : 0x7f80;
+    int e;
+    frexp(a, &e);                      /* a = m * 2^e, m in [0.5, 1) */
+    int q = e - 8;                     /* quantum of an 8-bit significand */
+    if (q < -133) q = -133;            /* subnormal bf16 quantum */
+    double n = nearbyint(ldexp(a, -q)); /* default mode: to nearest, ties even */
+    double r = ldexp(n, q);
+    if (r > 0x1.fep127)                /* rounded beyond the largest finite bf16 */
+        return neg ? 0xff80 : 0x7f80;
+    f = (float)r;                      /* exact: r has <= 8 significant bits */
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)((bits >> 16) | (neg ? 0x8000u : 0u));
+}
+
+/* ------------------------------------------------------------------ */
+/* Pack / unpack.                                                        */
+/* ------------------------------------------------------------------ */
+
+static int codes_per_word(int bits) { return 32 / bits; }
+
+/* Signed code of element k of one packed row. */
+static int unpack_one(const int32_t* row_words, int64_t k, int bits)
+{
+    int p = codes_per_word(bits);
+    uint32_t w = (uint32_t)row_words[k / p];
+    int j = (int)(k % p);
+    if (g_mutation == MUT_MSB_FIRST) j = p - 1 - j;
+    uint32_t field = (w >> (bits * j)) & ((1u << bits) - 1u);
+    int offset = 1 << (bits - 1);
+    if (g_mutation == MUT_CODE_OFFSET) offset -= 1;
+    return (int)field - offset;
+}
+
+/* codes int8 [rows, K] (values in [-2^(b-1), 2^(b-1)) ) -> words [rows, K/p].
+ * Returns 0, or -1 on a bad argument or an out-of-range code. */
+int oracle_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed)
+{
+    if (bits != 2 && bits != 4) return -1;
+    int p = codes_per_word(bits);
+    if (K % p) return -1;
+    int lo = -(1 << (bits - 1)), hi = (1 << (bits - 1)) - 1;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t wi = 0; wi < K / p; ++wi) {
+            uint32_t w = 0;
+            for (int j = 0; j < p; ++j) {
+                int c = codes[r * K + wi * p + j];
+                if (c < lo || c > hi) return -1;
+                uint32_t field = (uint32_t)(c - lo);
+                w |= field << (bits * j);
+            }
+            packed[r * (K / p) + wi] = (int32_t)w;
+        }
+    }
+    return 0;
+}
+
+int oracle_unpack(const int32_t* packed, int64_t rows, int64_t K, int bits, int8_t* codes)
+{
+    if (bits != 2 && bits != 4) return -1;
+    int p = codes_per_word(bits);
+    if (K % p) return -1;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t k = 0; k < K; ++k)
+            codes[r * K + k] = (int8_t)unpack_one(packed + r * (K / p), k, bits);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Dequantisation of whole rows (step 2).                                */
+/* ------------------------------------------------------------------ */
+
+static int64_t scale_index(int64_t k, int64_t group, int64_t n_groups)
+{
+    if (g_mutation == MUT_GROUP_AXIS) return k % n_groups;
+    return k / group;
+}
+
+/* One row: packed words [K/p], scales fp16 [K/group] -> BF16 values as double. */
+static void dequant_row(const int32_t* words, const uint16_t* scales, int64_t K,
+                        int64_t group, int bits, double* out)
+{
+    int64_t n_groups = K / group;
+    for (int64_t k = 0; k < K; ++k) {
+        int code = unpack_one(words, k, bits);
+        double s = oracle_fp16_to_double(scales[scale_index(k, group, n_groups)]);
+        /* code * s is exact in double; a single RNE step gives the BF16 weight */
+        out[k] = oracle_bf16_to_double(oracle_bf16_rne((double)code * s));
+    }
+}
+
+/* Public: dequantise [rows, K] to BF16 bit patterns (for the dequant pins). */
+int oracle_dequant(const int32_t* packed, const uint16_t* scales, int64_t rows, int64_t K,
+                   int64_t group, int bits, uint16_t* out_bf16)
+{
+    if (bits != 2 && bits != 4) return -1;
+    if (group <= 0 || K % group || K % codes_per_word(bits)) return -1;
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)K);
+    if (!tmp) return -1;
+    int p = codes_per_word(bits);
+    for (int64_t r = 0; r < rows; ++r) {
+        dequant_row(packed + r * (K / p), scales + r * (K / group), K, group, bits, tmp);
+        for (int64_t k = 0; k < K; ++k) out_bf16[r * K + k] = oracle_bf16_rne(tmp[k]);
+    }
+    free(tmp);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Routing lists (the "indexed" gather): counts, offsets, stable perm.    */
+/* ------------------------------------------------------------------ */
+
+/* ids int32 [R] (R = T*topk, flat slot f = t*topk + j).
+ * counts [E]; offsets [E+1] exclusive prefix; perm [R]: slots sorted by
+ * (expert, slot) ascending; inv [R]: inv[perm[i]] = i.
+ * Returns 0, or -1 if an id is outside [0, E). */
+int oracle_route(const int32_t* ids, int64_t R, int64_t E, int32_t* counts,
+                 int32_t* offsets, int32_t* perm, int32_t* inv)
+{
+    for (int64_t e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t f = 0; f < R; ++f) {
+        if (ids[f] < 0 || ids[f] >= E) return -1;
+        counts[ids[f]]++;
+    }
+    offsets[0] = 0;
+    for (int64_t e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    /* counting sort, one expert at a time, slots visited in ascending order */
+    for (int64_t e = 0; e < E; ++e) {
+        int32_t pos = offsets[e];
+        if (g_mutation == MUT_UNSTABLE_PERM) {
+            for (int64_t f = R - 1; f >= 0; --f)
+                if (ids[f] == e) perm[pos++] = (int32_t)f;
+        } else {
+            for (int64_t f = 0; f < R; ++f)
+                if (ids[f] == e) perm[pos++] = (int32_t)f;
+        }
+    }
+    for (int64_t i = 0; i < R; ++i) inv[perm[i]] = (int32_t)i;
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* The forward.                                                          */
+/* ------------------------------------------------------------------ */
+
+static double silu(double z)
+{
+    if (g_mutation == MUT_SILU_SIGN) return z / (1.0 + exp(z));
+    return z / (1.0 + exp(-z));
+}
+
+static float silu_f(float z)
+{
+    if (g_mutation == MUT_SILU_SIGN) return z / (1.0f + expf(z));
+    return z / (1.0f + expf(-z));
+}
+
+/* Clamped SwiGLU with limit L (L = +inf: no clamp). */
+static double swiglu(double g, double u, double L)
+{
+    if (g_mutation != MUT_NO_CLAMP) {
+        g = g < L ? g : L;             /* gate: clamped from above only */
+        u = u < -L ? -L : (u > L ? L : u);
+    }
+    return silu(g) * u;
+}
+
+static float swiglu_f(float g, float u, float L)
+{
+    if (g_mutation != MUT_NO_CLAMP) {
+        g = g < L ? g : L;
+        u = u < -L ? -L : (u > L ? L : u);
+    }
+    return silu_f(g) * u;
+}
+
+/*
+ * x        bf16 [T, K]          activations
+ * ids      int32 [T, topk]      expert of each slot
+ * wts      fp32 [T, topk]       routing weight of each slot
+ * w13p     int32 [E, 2N, K/p]   fused gate/up codes; rows [0,N) gate, [N,2N) up
+ * w13s     fp16  [E, 2N, K/g13]
+ * w2p      int32 [E, K, N/p]    down codes
+ * w2s      fp16  [E, K, N/g2]
+ * accum    0: fp64 dot products and combine; 1: fp32 (ascending order)
+ * tokens   optional list of n_tok token indices to evaluate (NULL: all T)
+ * out      bf16 [n_tok, K]
+ * h_out    optional bf16 [n_tok*topk, N]  (slot order t*topk + j)
+ * y_out    optional bf16 [n_tok*topk, K]
+ * Returns 0, or -1 on a bad argument / out-of-range expert id.
+ */
+int oracle_forward(const uint16_t* x, const int32_t* ids, const float* wts,
+                   const int32_t* w13p, const uint16_t* w13s,
+                   const int32_t* w2p, const uint16_t* w2s,
+                   int64_t T, int64_t K, int64_t N, int64_t E, int topk,
+                   int64_t g13, int64_t g2, int bits, float swiglu_limit, int accum,
+                   const int64_t* tokens, int64_t n_tok,
+                   uint16_t* out, uint16_t* h_out, uint16_t* y_out)
+{
+    if (bits != 2 && bits != 4) return -1;
+    int p = codes_per_word(bits);
+    if (K % p || N % p || g13 <= 0 || g2 <= 0 || K % g13 || N % g2 || topk <= 0) return -1;
+    if (!tokens) n_tok = T;
+    for (int64_t i = 0; i < n_tok; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) return -1;
+        for (int j = 0; j < topk; ++j)
+            if (ids[t * topk + j] < 0 || ids[t * topk + j] >= E) return -1;
+    }
+    const double L = (double)swiglu_limit;
+    const int64_t R = n_tok * topk;
+
+    /* Slots of the selected tokens, grouped by expert only so that each
+     * expert's weights are dequantised once; every output element is still
+     * one dot product in ascending order, so the result does not depend on
+     * this grouping or on the thread count. */
+    double* W13 = (double*)malloc(sizeof(double) * (size_t)(2 * N * K));
+    double* W2 = (double*)malloc(sizeof(double) * (size_t)(K * N));
+    double* hbuf = (double*)malloc(sizeof(double) * (size_t)(R * N)); /* bf16 values */
+    double* ybuf = (double*)malloc(sizeof(double) * (size_t)(R * K)); /* bf16 values */
+    double* xrow = (double*)malloc(sizeof(double) * (size_t)(n_tok * K));
+    if (!W13 || !W2 || !hbuf || !ybuf || !xrow) {
+        free(W13); free(W2); free(hbuf); free(ybuf); free(xrow);
+        return -1;
+    }
+    for (int64_t i = 0; i < n_tok; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        for (int64_t k = 0; k < K; ++k) xrow[i * K + k] = oracle_bf16_to_double(x[t * K + k]);
+    }
+
+    for (int64_t e = 0; e < E; ++e) {
+        int used = 0;
+        for (int64_t s = 0; s < R && !used; ++s) {
+            int64_t t = tokens ? tokens[s / topk] : s / topk;
+            used = ids[t * topk + s % topk] == e;
+        }
+        if (!used) continue;
+
+        /* step 2 for this expert */
+        #pragma omp parallel for schedule(static)
+        for (int64_t r = 0; r < 2 * N; ++r)
+            dequant_row(w13p + (e * 2 * N + r) * (K / p), w13s + (e * 2 * N + r) * (K / g13),
+                        K, g13, bits, W13 + r * K);
+        #pragma omp parallel for schedule(static)
+        for (int64_t m = 0; m < K; ++m)
+            dequant_row(w2p + (e * K + m) * (N / p), w2s + (e * K + m) * (N / g2),
+                        N, g2, bits, W2 + m * N);
+
+        for (int64_t s = 0; s < R; ++s) {
+            int64_t i = s / topk;
+            int64_t t = tokens ? tokens[i] : i;
+            if (ids[t * topk + s % topk] != e) continue;
+            const double* xs = xrow + i * K;
+            int64_t gate0 = 0, up0 = N;
+            if (g_mutation == MUT_GATE_UP_SWAP) { gate0 = N; up0 = 0; }
+
+            /* steps 4 and 5: h = swiglu(W1 x, W3 x), rounded to bf16 */
+            #pragma omp parallel for schedule(static)
+            for (int64_t n = 0; n < N; ++n) {
+                const double* w1 = W13 + (gate0 + n) * K;
+                const double* w3 = W13 + (up0 + n) * K;
+                if (accum == 0) {
+                    double g = 0.0, u = 0.0;
+                    for (int64_t k = 0; k < K; ++k) { g += w1[k] * xs[k]; u += w3[k] * xs[k]; }
+                    hbuf[s * N + n] = oracle_bf16_to_double(oracle_bf16_rne(swiglu(g, u, L)));
+                } else {
+                    float g = 0.0f, u = 0.0f;
+                    for (int64_t k = 0; k < K; ++k) {
+                        g += (float)w1[k] * (float)xs[k];
+                        u += (float)w3[k] * (float)xs[k];
+                    }
+                    hbuf[s * N + n] = oracle_bf16_to_double(
+                        oracle_bf16_rne((double)swiglu_f(g, u, (float)L)));
+                }
+            }
+            /* step 6: y = W2 h, rounded to bf16 */
+            #pragma omp parallel for schedule(static)
+            for (int64_t m = 0; m < K; ++m) {
+                const double* hs = hbuf + s * N;
+                if (accum == 0) {
+                    double acc = 0.0;
+                    if (g_mutation == MUT_W2_TRANSPOSE) {
+                        /* reads the [K, N] tensor as if it were [N, K] */
+                        for (int64_t n = 0; n < N; ++n) acc += W2[n * K + m] * hs[n];
+                    } else {
+                        for (int64_t n = 0; n < N; ++n) acc += W2[m * N + n] * hs[n];
+                    }
+                    ybuf[s * K + m] = oracle_bf16_to_double(oracle_bf16_rne(acc));
+                } else {
+                    float acc = 0.0f;
+                    for (int64_t n = 0; n < N; ++n) acc += (float)W2[m * N + n] * (float)hs[n];
+                    ybuf[s * K + m] = oracle_bf16_to_double(oracle_bf16_rne((double)acc));
+                }
+            }
+        }
+    }
+
+    /* step 7: combine, j ascending */
+    for (int64_t i = 0; i < n_tok; ++i) {
+        int64_t t = tokens ? tokens[i] : i;
+        for (int64_t m = 0; m < K; ++m) {
+            if (accum == 0) {
+                double acc = 0.0;
+                for (int j = 0; j < topk; ++j) {
+                    double wj = g_mutation == MUT_NO_ROUTE_WEIGHT ? 1.0 : (double)wts[t * topk + j];
+                    acc += wj * ybuf[(i * topk + j) * K + m];
+                }
+                out[i * K + m] = oracle_bf16_rne(acc);
+            } else {
+                float acc = 0.0f;
+                for (int j = 0; j < topk; ++j) {
+                    float wj = g_mutation == MUT_NO_ROUTE_WEIGHT ? 1.0f : wts[t * topk + j];
+                    acc += wj * (float)ybuf[(i * topk + j) * K + m];
+                }
+                out[i * K + m] = oracle_bf16_rne((double)acc);
+            }
+        }
+    }
+    if (h_out)
+        for (int64_t q = 0; q < R * N; ++q) h_out[q] = oracle_bf16_rne(hbuf[q]);
+    if (y_out)
+        for (int64_t q = 0; q < R * K; ++q) y_out[q] = oracle_bf16_rne(ybuf[q]);
+
+    free(W13); free(W2); free(hbuf); free(ybuf); free(xrow);
+    return 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,335 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each pin checks the oracle against a fact fixed by the pages' format
+definition or by mathematics: hand-decoded words, exact rational rounding,
+closed-form SwiGLU cases, a library routine (numpy stable sort, torch
+matmul/silu) on a special case, invariants (zero codes, scale doubling,
+relabelling, token permutation) and a pure-Python brute force on tiny inputs.
+``test_every_planted_mistake_is_caught`` plants each plausible bug in the
+oracle and checks that at least one pin fails.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import independent as ind
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- helpers
+
+def _tiny_case(bits, T=3, K=64, N=32, E=3, topk=2, g13=16, g2=16, seed=11, scale=(0.05, 0.3)):
+    rng = np.random.default_rng(seed)
+    p = 32 // bits
+    w13p = rng.integers(0, 1 << 32, size=(E, 2 * N, K // p), dtype=np.uint32).view(np.int32)
+    w2p = rng.integers(0, 1 << 32, size=(E, K, N // p), dtype=np.uint32).view(np.int32)
+    w13s = rng.uniform(*scale, size=(E, 2 * N, K // g13)).astype(np.float16)
+    w2s = rng.uniform(*scale, size=(E, K, N // g2)).astype(np.float16)
+    x = synth.to_bf16_bits(rng.standard_normal((T, K), dtype=np.float32))
+    logits = rng.standard_normal((T, E), dtype=np.float32)
+    ids, wts = synth.route_topk(logits, topk)
+    return dict(x=x, ids=ids, weights=wts, w13_packed=w13p, w13_scales=w13s, w2_packed=w2p,
+                w2_scales=w2s, K=K, N=N, E=E, topk=topk, g13=g13, g2=g2, bits=bits)
+
+
+def _run(oracle, c, limit=7.0, **kw):
+    return oracle.forward(c["x"], c["ids"], c["weights"], c["w13_packed"], c["w13_scales"],
+                          c["w2_packed"], c["w2_scales"], bits=c["bits"], group_size=c["g13"],
+                          group_size_w2=c["g2"], swiglu_limit=limit, **kw)
+
+
+def _bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- pins
+
+def pin_fp16_decode(oracle):
+    """fp16 -> double equals numpy's float16 conversion for every pattern."""
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = allbits.view(np.float16).astype(np.float64)
+    for b in list(range(0, 1 << 16, 97)) + [0x0001, 0x03FF, 0x0400, 0x7BFF, 0x8001, 0xFBFF, 0x3C00]:
+        if np.isnan(ref[b]):
+            continue
+        assert oracle.fp16_to_double(b) == ref[b], hex(b)
+
+
+def pin_bf16_rounding(oracle):
+    """One-step RNE to bf16: exact-rational reference and torch's fp32->bf16."""
+    rng = np.random.default_rng(5)
+    vals = list(rng.standard_normal(300) * np.exp(rng.uniform(-20, 20, 300)))
+    # ties and near-ties around 1: 1 + 2^-8 is a tie (-> 1.0, even); a hair above goes up
+    vals += [1 + 2.0 ** -8, 1 + 3 * 2.0 ** -8, 1 + 2.0 ** -8 + 2.0 ** -30, -(1 + 2.0 ** -8),
+             2.0 ** -130, 3 * 2.0 ** -134, 3.3895313892515355e38, 3.4e38, 1e-45]
+    for v in vals:
+        assert oracle.bf16_rne(v) == ind.bf16_bits_exact(v), v
+    f32 = rng.standard_normal(2000).astype(np.float32)
+    tb = torch.from_numpy(f32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    for v, b in zip(f32, tb):
+        assert oracle.bf16_rne(float(v)) == int(b)
+
+
+def pin_hand_words(oracle):
+    with open(os.path.join(GOLDEN, "packed_words.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        bits = c["bits"]
+        p = 32 // bits
+        word = np.array([[int(c["word"], 16)]], dtype=np.uint32).view(np.int32)
+        got = oracle.unpack(word, p, bits)[0].tolist()
+        assert got == c["codes"], c
+        assert oracle.pack(np.array([c["codes"]], np.int8), bits).view(np.uint32)[0, 0] == int(c["word"], 16)
+
+
+def pin_pack_roundtrip(oracle):
+    rng = np.random.default_rng(3)
+    for bits in (2, 4):
+        codes = synth.random_codes(rng, (7, 128), bits)
+        words = oracle.pack(codes, bits)
+        assert np.array_equal(oracle.unpack(words, 128, bits), codes)
+        raw = rng.integers(0, 1 << 32, size=(5, 8), dtype=np.uint32).view(np.int32)
+        K = 8 * 32 // bits
+        assert np.array_equal(oracle.pack(oracle.unpack(raw, K, bits), bits), raw)
+        # independent Python unpacking agrees
+        for r in range(5):
+            ref = []
+            for wi in range(8):
+                ref += ind.py_unpack_word(int(raw[r, wi]), bits)
+            assert oracle.unpack(raw[r:r + 1], K, bits)[0].tolist() == ref
+
+
+def pin_dequant(oracle):
+    """bf16(code*scale) with exact rational rounding; W2 == code*bf16(scale)."""
+    rng = np.random.default_rng(7)
+    for bits, group in ((2, 32), (4, 16), (4, 64)):
+        K = 128
+        p = 32 // bits
+        words = rng.integers(0, 1 << 32, size=(4, K // p), dtype=np.uint32).view(np.int32)
+        scales = rng.uniform(0.001, 0.02, size=(4, K // group)).astype(np.float16)
+        got = oracle.dequant(words, scales, K, group, bits)
+        sbits = scales.view(np.uint16)
+        for r in range(4):
+            codes = []
+            for wi in range(K // p):
+                codes += ind.py_unpack_word(int(words[r, wi]), bits)
+            for k in range(K):
+                from fractions import Fraction
+                s = Fraction(ind.fp16_value(int(sbits[r, k // group])))
+                assert got[r, k] == ind.bf16_bits_exact(codes[k] * s), (bits, r, k)
+                if bits == 2:
+                    sb = ind.bf16_value(ind.bf16_bits_exact(s))
+                    assert ind.bf16_value(int(got[r, k])) == codes[k] * sb
+
+
+def pin_route(oracle):
+    rng = np.random.default_rng(9)
+    for R, E in ((64, 8), (1000, 37), (7, 256)):
+        ids = rng.integers(0, E, size=R).astype(np.int32)
+        counts, offsets, perm, inv = oracle.route(ids, E)
+        assert np.array_equal(counts, np.bincount(ids, minlength=E))
+        assert offsets[0] == 0 and offsets[-1] == R
+        assert np.array_equal(perm, np.argsort(ids, kind="stable"))
+        assert np.array_equal(inv[perm], np.arange(R))
+
+
+def pin_zero_codes(oracle):
+    """All-zero codes (stored 0xAAAAAAAA / 0x88888888) give exactly +0."""
+    for bits, word in ((2, 0xAAAAAAAA), (4, 0x88888888)):
+        c = _tiny_case(bits)
+        c["w13_packed"] = np.full_like(c["w13_packed"], np.uint32(word).view(np.int32))
+        c["w2_packed"] = np.full_like(c["w2_packed"], np.uint32(word).view(np.int32))
+        out = _run(oracle, c)
+        assert np.all(out == 0), bits
+
+
+def pin_brute_force(oracle):
+    """Pure-Python loops on tiny inputs give the same bits (fp64 mode)."""
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=2, K=32, N=16, E=3, topk=2, g13=8, g2=8)
+        got = _run(oracle, c)
+        ref = ind.brute_force_forward(
+            c["x"], c["ids"], c["weights"], c["w13_packed"], c["w13_scales"].view(np.uint16),
+            c["w2_packed"], c["w2_scales"].view(np.uint16), c["K"], c["N"], c["E"], c["topk"],
+            c["g13"], c["g2"], bits, 7.0)
+        assert np.array_equal(got, ref), bits
+
+
+def _dense_mlp_torch(c, limit):
+    """One expert, top-1, weight 1: a plain dense SwiGLU MLP in torch fp64 on the
+    dequantised weights (numpy unpacking, torch bf16 rounding)."""
+    bits = c["bits"]
+    p = 32 // bits
+
+    def deq(words, scales, group):
+        w = words.view(np.uint32)[..., None] >> (bits * np.arange(p, dtype=np.uint32))
+        codes = (w & ((1 << bits) - 1)).astype(np.int64).reshape(words.shape[0], -1) - (1 << (bits - 1))
+        s = np.repeat(scales.astype(np.float64), group, axis=1)
+        prod = torch.from_numpy(codes.astype(np.float64) * s).to(torch.float32)  # exact
+        return prod.to(torch.bfloat16).to(torch.float64)
+
+    W13 = deq(c["w13_packed"][0], c["w13_scales"][0], c["g13"])
+    W2 = deq(c["w2_packed"][0], c["w2_scales"][0], c["g2"])
+    x = torch.from_numpy(_bf16_to_f64(c["x"]))
+    N = c["N"]
+    gu = x @ W13.T
+    g, u = gu[:, :N], gu[:, N:]
+    h = (torch.nn.functional.silu(torch.clamp(g, max=limit)) * torch.clamp(u, -limit, limit))
+    h = h.to(torch.float32).to(torch.bfloat16).to(torch.float64)
+    y = (h @ W2.T).to(torch.float32).to(torch.bfloat16)
+    return y.view(torch.int16).numpy().view(np.uint16)
+
+
+def pin_dense_mlp(oracle):
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=6, K=64, N=32, E=1, topk=1, g13=16, g2=32, scale=(0.05, 0.4))
+        c["ids"] = np.zeros((6, 1), np.int32)
+        c["weights"] = np.ones((6, 1), np.float32)
+        got = _run(oracle, c, limit=7.0)
+        ref = _dense_mlp_torch(c, 7.0)
+        # torch rounds through fp32 (two roundings); allow a rare one-ulp flip
+        diff = np.abs(got.astype(np.int32) - ref.astype(np.int32))
+        assert diff.max() <= 1 and (diff == 0).mean() > 0.97, (bits, diff.max(), (diff == 0).mean())
+        assert np.abs(_bf16_to_f64(got)).max() > 0
+
+
+def _clamp_case(gate_code, gate_scale, up_code, up_scale):
+    """E=1, top-1, K=N=16, 2-bit, group 16: x = e_0, so g = gate_code*gate_scale,
+    u = up_code*up_scale in row 0, every other h is 0, and each w2 row copies h_0."""
+    K = N = 16
+    bits = 2
+
+    def word(code0):
+        codes = np.zeros((1, 16), np.int8)
+        codes[0, 0] = code0
+        return codes
+
+    import oracle as o
+    zero = o.pack(np.zeros((1, 16), np.int8), bits)[0, 0]
+    w13 = np.full((1, 2 * N, 1), zero, np.int32)
+    w13[0, 0, 0] = o.pack(word(gate_code), bits)[0, 0]
+    w13[0, N, 0] = o.pack(word(up_code), bits)[0, 0]
+    w13s = np.ones((1, 2 * N, 1), np.float16)
+    w13s[0, 0, 0] = gate_scale
+    w13s[0, N, 0] = up_scale
+    w2 = np.full((1, K, 1), o.pack(word(1), bits)[0, 0], np.int32)
+    w2s = np.ones((1, K, 1), np.float16)
+    x = np.zeros((1, K), np.float32)
+    x[0, 0] = 1.0
+    return dict(x=synth.to_bf16_bits(x), ids=np.zeros((1, 1), np.int32), weights=np.ones((1, 1), np.float32),
+                w13_packed=w13, w13_scales=w13s, w2_packed=w2, w2_scales=w2s, K=K, N=N, E=1, topk=1,
+                g13=16, g2=16, bits=bits)
+
+
+def pin_clamp_closed_form(oracle):
+    L = 7.0
+    silu = lambda z: z / (1.0 + math.exp(-z))  # noqa: E731
+    cases = [
+        ((1, 10.0, 1, 1.0), silu(7.0) * 1.0),      # gate 10 is clamped to 7
+        ((1, 1.0, -1, 10.0), silu(1.0) * -7.0),    # up -10 is clamped to -7
+        ((-1, 10.0, 1, 1.0), silu(-10.0) * 1.0),   # gate -10 is not clamped
+        ((1, 2.0, 1, 8.0), silu(2.0) * 7.0),       # up 8 is clamped to 7
+        ((1, 0.5, -2, 1.5), silu(0.5) * -3.0),     # inside the limits
+    ]
+    for args, h0 in cases:
+        c = _clamp_case(*args)
+        out = _run(oracle, c, limit=L)
+        expect = ind.bf16_bits_exact(ind.bf16_value(ind.bf16_bits_exact(h0)))
+        assert np.all(out[0] == expect), (args, out[0][:2], expect)
+    # no limit (+inf): gate 10 passes through
+    c = _clamp_case(1, 10.0, 1, 1.0)
+    out = _run(oracle, c, limit=float("inf"))
+    assert np.all(out[0] == ind.bf16_bits_exact(silu(10.0)))
+
+
+def pin_scale_doubling(oracle):
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=4, K=64, N=32, E=3, topk=2)
+        out = _run(oracle, c)
+        c2 = dict(c)
+        c2["w2_scales"] = (c["w2_scales"].astype(np.float32) * 2).astype(np.float16)
+        out2 = _run(oracle, c2)
+        assert np.array_equal(_bf16_to_f64(out2), 2 * _bf16_to_f64(out))
+
+
+def pin_relabel_and_token_permutation(oracle):
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=5, K=64, N=32, E=4, topk=2)
+        out = _run(oracle, c)
+        sigma = np.array([2, 0, 3, 1])        # new label of old expert e is sigma[e]
+        c2 = dict(c)
+        for key in ("w13_packed", "w13_scales", "w2_packed", "w2_scales"):
+            arr = np.empty_like(c[key])
+            arr[sigma] = c[key]
+            c2[key] = arr
+        c2["ids"] = sigma[c["ids"]].astype(np.int32)
+        assert np.array_equal(_run(oracle, c2), out)
+        tp = np.array([3, 0, 4, 2, 1])
+        c3 = dict(c, x=c["x"][tp], ids=c["ids"][tp], weights=c["weights"][tp])
+        assert np.array_equal(_run(oracle, c3), out[tp])
+
+
+def pin_split_routing_weight(oracle):
+    """Two slots on the same expert with weights 0.25 and 0.75 equal one slot of
+    weight 1 (the sum w*y + (1-w)*y is exact here), and weight 0.5 halves it."""
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=3, K=64, N=32, E=3, topk=2)
+        c1 = dict(c, ids=c["ids"][:, :1].copy(), weights=np.ones((3, 1), np.float32), topk=1)
+        one = _run(oracle, c1)
+        c2 = dict(c, ids=np.repeat(c["ids"][:, :1], 2, axis=1),
+                  weights=np.tile(np.array([[0.25, 0.75]], np.float32), (3, 1)))
+        assert np.array_equal(_run(oracle, c2), one)
+        c3 = dict(c1, weights=np.full((3, 1), 0.5, np.float32))
+        assert np.array_equal(_bf16_to_f64(_run(oracle, c3)), 0.5 * _bf16_to_f64(one))
+
+
+PINS = [pin_fp16_decode, pin_bf16_rounding, pin_hand_words, pin_pack_roundtrip, pin_dequant,
+        pin_route, pin_zero_codes, pin_brute_force, pin_dense_mlp, pin_clamp_closed_form,
+        pin_scale_doubling, pin_relabel_and_token_permutation, pin_split_routing_weight]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(clean_oracle, pin):
+    pin(clean_oracle)
+
+
+@pytest.mark.parametrize("mutation", sorted(__import__("oracle").MUTATIONS))
+def test_every_planted_mistake_is_caught(clean_oracle, mutation):
+    clean_oracle.set_mutation(mutation)
+    failed = []
+    for pin in PINS:
+        try:
+            pin(clean_oracle)
+        except (AssertionError, Exception) as exc:  # noqa: B014 - any failure counts
+            failed.append((pin.__name__, type(exc).__name__))
+    assert failed, f"no pin caught mutation {mutation}"
+
+
+def test_fp32_mode_close_to_fp64(clean_oracle):
+    c = _tiny_case(4, T=8, K=256, N=128, E=4, topk=2, g13=128, g2=64)
+    a = _run(clean_oracle, c)
+    b = _run(clean_oracle, c, accum="fp32")
+    diff = np.abs(a.astype(np.int32) - b.astype(np.int32))
+    assert (diff == 0).mean() > 0.95 and diff.max() <= 2
+
+
+def test_token_subset_matches_full(clean_oracle):
+    c = _tiny_case(2, T=6, K=64, N=32, E=3, topk=2)
+    full = _run(clean_oracle, c)
+    sub = _run(clean_oracle, c, tokens=np.array([4, 1]))
+    assert np.array_equal(sub, full[[4, 1]])
+
+
+def test_out_of_range_id_is_an_error(clean_oracle):
+    c = _tiny_case(2)
+    c["ids"] = c["ids"].copy()
+    c["ids"][0, 0] = c["E"]
+    with pytest.raises(clean_oracle.OracleError):
+        _run(clean_oracle, c)
