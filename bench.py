@@ -1,0 +1,399 @@
+"""Benchmark of the WNA16 routed-expert MoE forward on GB300.
+
+One step = one full forward (route -> gather -> w13 GEMM + SwiGLU -> w2 GEMM
+-> combine) over one batch of synthetic, seeded inputs that are resident in
+HBM.  L2 is flushed (a 512 MiB write) before every timed step, outside the
+timed region; each step is timed with CUDA events on the launching stream.
+
+Default workload: decode, 4 concurrent sequences one step (T=4), hidden 4096,
+intermediate 2048, 256 experts, top-8, W2A16 with group 128.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own
+batch (weak scaling, no collective on the data path); the step time is the
+max over ranks.  `--impl reference` times the CPU oracle (the plain C
+definition of the forward) on the host cores instead.
+Prints ONE JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------ workload facts
+
+def active_experts(ids: np.ndarray, E: int) -> int:
+    return int(np.count_nonzero(np.bincount(ids.ravel(), minlength=E)))
+
+
+def algorithmic(w: synth.Workload, ids: np.ndarray) -> dict:
+    """Algorithmic bytes / flops (real rows only, intermediates not counted)."""
+    n_act = active_experts(ids, w.E)
+    p = 32 // w.bits
+    w13_bytes = 2 * w.N * (w.K // p) * 4 + 2 * w.N * (w.K // w.g13) * 2      # packed + scales per expert
+    w2_bytes = w.K * (w.N // p) * 4 + w.K * (w.N // w.g2) * 2
+    R = w.T * w.topk
+    return dict(
+        active_experts=n_act,
+        w13_kernel_bytes=n_act * w13_bytes + w.T * w.K * 2 + R * w.N * 2,   # weights + x in + h out
+        w2_kernel_bytes=n_act * w2_bytes + R * w.N * 2 + R * w.K * 2,       # weights + h in + y out
+        forward_bytes=n_act * (w13_bytes + w2_bytes) + 2 * w.T * w.K * 2 + w.T * w.topk * 8,
+        w13_flops=4.0 * R * w.N * w.K,
+        w2_flops=2.0 * R * w.N * w.K,
+        forward_flops=6.0 * R * w.N * w.K,
+    )
+
+
+def is_decode(w: synth.Workload) -> bool:
+    return w.T * w.topk <= 4 * w.E
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+
+        def pick(*keys):
+            for k in keys:
+                if k in pk and isinstance(pk[k], (int, float)):
+                    return float(pk[k]), "measured"
+            return None, None
+        hbm, src = pick("hbm_gbs", "hbm_copy_gbs")
+        bf16, _ = pick("bf16_tflops")
+        if hbm and bf16:
+            return dict(hbm_gbs=hbm, bf16_tflops=bf16, source="measured (MEASURED_PEAKS.json)")
+    return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "wna16_grouped_gemm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    e = rec.get(workload, {}).get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), reasons=sorted(reasons), samples=len(sm))
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def time_oracle(w: synth.Workload, inp: dict, budget_s: float, min_runs: int = 1, max_tokens: int | None = None):
+    """Run the oracle forward on a bounded token sample; returns (tokens/s, sample text, cores, seconds)."""
+    import oracle
+    oracle.build()
+    toks = None
+    n_tok = w.T
+    if max_tokens is not None and w.T > max_tokens:
+        toks = np.linspace(0, w.T - 1, max_tokens).astype(np.int64)
+        n_tok = max_tokens
+    runs = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.forward(inp["x"], inp["ids"], inp["weights"], inp["w13_packed"], inp["w13_scales"], inp["w2_packed"],
+                       inp["w2_scales"], bits=w.bits, group_size=w.g13, group_size_w2=w.g2,
+                       swiglu_limit=w.swiglu_limit, tokens=toks)
+        runs += 1
+        el = time.perf_counter() - t0
+        if runs >= min_runs and el >= budget_s:
+            break
+    sample = f"{runs} oracle forward(s) of {n_tok} of {w.T} tokens ({'all' if toks is None else 'evenly spaced'})"
+    return runs * n_tok / el, sample, oracle.num_threads(), el
+
+
+# ------------------------------------------------------------------ main
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="decode_w2")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--oracle-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = os.environ.get("WNA16_BENCH_BACKEND", "nccl")
+        dist.init_process_group(backend)
+        return rank, world, local, dist
+    return 0, 1, 0, None
+
+
+def run_reference(args, w, rank, world, dist):
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+    inp = synth.make_all(w, args.seed)
+    max_tok = None if w.T <= 16 else 8
+    per_step = max(1.0, args.oracle_seconds / max(1, args.steps))
+    times = []
+    rate = None
+    for i in range(args.warmup + args.steps):
+        r, sample, cores, el = time_oracle(w, inp, per_step if i >= args.warmup else 0.0, 1, max_tok)
+        if i >= args.warmup:
+            times.append(el)
+            rate = r if rate is None else rate
+    tok_per_step = w.T if max_tok is None else max_tok
+    tot = sum(times)
+    value = tok_per_step * args.steps / tot if tot > 0 else 0.0
+    line = dict(impl="reference", metric="routed-MoE tokens/s (W2/W4A16 WNA16 forward)", value=value,
+                unit="tokens/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+                ms_per_step=1000.0 * tot / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
+                dtype="f64", data="synthetic", config=workload_config(w),
+                cpu_baseline=dict(value=value, unit="tokens/s", cores=cores, kind="oracle", sample=sample),
+                e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
+    print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+def workload_config(w):
+    return dict(workload=w.name, T=w.T, hidden=w.K, intermediate=w.N, experts=w.E, topk=w.topk, bits=w.bits,
+                group_w13=w.g13, group_w2=w.g2, swiglu_limit=w.swiglu_limit,
+                routing="softmax top-k of N(0,1) logits" + (f" + Zipf({w.zipf_s}) bias" if w.zipf_s else ""),
+                l2="flushed before every timed step (512 MiB write)", weights="resident in HBM")
+
+
+def main():
+    args = parse()
+    w = synth.get(args.workload)
+    rank, world, local, dist = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, w, rank, world, dist)
+
+    import torch
+    import wna16_grouped_gemm_gb300 as moe
+    from wna16_grouped_gemm_gb300 import build
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        build.build()
+    if dist:
+        dist.barrier()
+    dev = torch.device("cuda", local)
+    inp = synth.make_all(w, args.seed + rank)
+    facts = algorithmic(w, inp["ids"])
+
+    x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    ids = torch.from_numpy(inp["ids"]).to(dev)
+    wts = torch.from_numpy(inp["weights"]).to(dev)
+    w13p = torch.from_numpy(inp["w13_packed"]).to(dev)
+    w13s = torch.from_numpy(inp["w13_scales"]).to(dev)
+    w2p = torch.from_numpy(inp["w2_packed"]).to(dev)
+    w2s = torch.from_numpy(inp["w2_scales"]).to(dev)
+    ws = moe.alloc_workspace(w.T, w.K, w.N, w.E, w.topk, w.bits, dev)
+    out = torch.empty(w.T, w.K, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd(xx=x, ii=ids, ww=wts, oo=out):
+        moe.forward(xx, ii, ww, w13p, w13s, w2p, w2s, bits=w.bits, group_size=w.g13, group_size_w2=w.g2,
+                    swiglu_limit=w.swiglu_limit, out=oo, workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        fwd()
+    torch.cuda.synchronize()
+    if moe.read_status(ws) != moe.OK:
+        raise SystemExit(f"device status {moe.read_status(ws)} after warm-up")
+
+    # ---- device-resident timed region
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = {k: [] for k in moe.binding.STAGES}
+    moe.profile(args.steps)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            fwd()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    for rec in moe.profile_read(args.steps):
+        for k, v in rec.items():
+            stage_ms[k].append(v)
+    moe.profile(0)
+    if dist:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / len(step_ms)
+    status = moe.read_status(ws)
+    if status != moe.OK:
+        raise SystemExit(f"device status {status} in timed region")
+
+    # ---- end to end through the public API with host buffers
+    x_h = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    ids_h = torch.from_numpy(inp["ids"]).pin_memory()
+    wts_h = torch.from_numpy(inp["weights"]).pin_memory()
+    out_h = torch.empty(w.T, w.K, dtype=torch.bfloat16).pin_memory()
+    xd, idd, wd = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(wts)
+    e_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e_st[i].record(stream)
+        xd.copy_(x_h, non_blocking=True)
+        idd.copy_(ids_h, non_blocking=True)
+        wd.copy_(wts_h, non_blocking=True)
+        fwd(xd, idd, wd, out)
+        out_h.copy_(out, non_blocking=True)
+        e_en[i].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_st, e_en)) / args.steps
+    h2d = x_h.numel() * 2 + ids_h.numel() * 4 + wts_h.numel() * 4
+    d2h = out_h.numel() * 2
+
+    # ---- max over ranks
+    if dist:
+        t = torch.tensor([ms, e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+
+    if rank == 0:
+        peaks = load_peaks()
+        st = {k: (sum(v) / len(v) if v else 0.0) for k, v in stage_ms.items()}
+        decode = is_decode(w)
+        dom = "w13" if st["w13"] >= st["w2"] else "w2"
+        dom_ms = st[dom]
+        if decode:
+            achieved = facts[f"{dom}_kernel_bytes"] / (dom_ms * 1e-3) / 1e9
+            roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                        frac=achieved / peaks["hbm_gbs"])
+        else:
+            achieved = facts[f"{dom}_flops"] / (dom_ms * 1e-3) / 1e12
+            roof = dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                        frac=achieved / peaks["bf16_tflops"])
+        roof.update(kernel=f"grouped_gemm_{dom}", peak_source=peaks["source"],
+                    algorithmic_per_launch=facts[f"{dom}_kernel_bytes"] if decode else facts[f"{dom}_flops"],
+                    traffic=recorded_traffic(w.name, dom))
+        tokens = w.T * world
+        line = dict(
+            metric="routed-MoE tokens/s (W2/W4A16 WNA16 forward)",
+            value=tokens / (ms * 1e-3), unit="tokens/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
+            ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+            data="synthetic", config=workload_config(w), roofline=roof,
+            forward=dict(hbm_gbs=facts["forward_bytes"] / (ms * 1e-3) / 1e9,
+                         hbm_frac=facts["forward_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         tflops=facts["forward_flops"] / (ms * 1e-3) / 1e12,
+                         tensor_frac=facts["forward_flops"] / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                         algorithmic_bytes=facts["forward_bytes"], active_experts=facts["active_experts"],
+                         stage_ms=st, step_ms_median=statistics.median(step_ms)),
+            e2e=dict(value=tokens / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=h2d,
+                     d2h_bytes_per_step=d2h, ms_per_step=e2e_ms),
+            gpu_launches=5 * args.steps * world,
+            clocks=clk.summary(),
+        )
+        if not args.no_cpu_baseline:
+            max_tok = None if w.T <= 16 else 8
+            rate, sample, cores, _ = time_oracle(w, inp, args.oracle_seconds, 1, max_tok)
+            line["cpu_baseline"] = dict(value=rate, unit="tokens/s", cores=cores, kind="oracle", sample=sample)
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * wna16_moe.h -- C ABI of the GB300 (sm_103a) WNA16 routed-expert MoE forward.
+ *
+ * The operation is the indexed routed-expert MoE of the page "Incubate
+ * DeepSeek V4 WNA16 runtime on SM86" (section "What this branch adds": items 1
+ * "symmetric W2A16 compressed-tensors MoE loading", 2 "separate WNA16 schemas
+ * for fused gate/up (w13) and down (w2)", 3 "W2, group-128, BF16 indexed MoE",
+ * 9 "SwiGLU alpha, beta, and clamp semantics ... corrected N/K group-shape
+ * metadata"), on the weight format of the page
+ * "hampsonw/DeepSeek-V4-Flash-0731-WNA16" (section "What changed": symmetric
+ * W2A16 with group size 128, "FP16 group scales and INT32 packed values";
+ * section "How it was created", step 4: signed codes packed with
+ * compressed-tensors).  4-bit experts follow the page "DeepSeek-V4-Flash-
+ * W4A16-FP8-MTP -- Ada (SM89) Serving Edition" (section "What this checkpoint
+ * is": "W4A16 INT4 experts").
+ *
+ * Notation: T tokens, K hidden size, N intermediate size, E experts, topk
+ * slots per token, b = bits (2 or 4), p = 32/b codes per INT32 word,
+ * R = T*topk routed slots (slot f = t*topk + j).
+ *
+ * Formats (all tensors row-major and contiguous):
+ *   x            bf16  [T, K]
+ *   topk_ids     int32 [T, topk]       expert of each slot, in [0, E)
+ *   topk_weights fp32  [T, topk]
+ *   w13_packed   int32 [E, 2N, K/p]    rows [0, N) gate (w1), rows [N, 2N) up (w3)
+ *   w13_scales   fp16  [E, 2N, K/g13]  one scale per group of g13 consecutive k
+ *   w2_packed    int32 [E, K, N/p]
+ *   w2_scales    fp16  [E, K, N/g2]
+ *   out          bf16  [T, K]
+ * Word layout: element k of a row is field (k mod p) of word (k / p), field j
+ * at bits [b*j, b*j + b) (least significant first); the field stores
+ * code + 2^(b-1), code in [-2^(b-1), 2^(b-1)).  Dequantised weight:
+ * bf16_rne(code * scale), exact product rounded once.
+ *
+ * Semantics (per slot f = t*topk + j, e = topk_ids[t][j]):
+ *   g = W1_e x_t,  u = W3_e x_t                      (fp32 accumulation)
+ *   h = bf16( silu(min(g, L)) * clamp(u, -L, L) )    L = swiglu_limit (+inf: no clamp)
+ *   y = bf16( W2_e h )
+ *   out_t = bf16( sum_j topk_weights[t][j] * y_f )  (fp32, j ascending)
+ *
+ * Conventions for every call:
+ *   - Tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or retains them.  Scratch comes from `workspace`
+ *     (size from wna16_moe_workspace_size), also owned by the caller.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  The return value reports host-side validation and
+ *     launch errors only; device-side conditions (an expert id outside
+ *     [0, E), a pipeline wait that timed out) are written to a status word in
+ *     the workspace and read with wna16_moe_read_status.
+ *   - On any non-zero return nothing has been launched, except
+ *     WNA16_ERR_CUDA, which reports a failed launch.
+ *   - Thread safety: calls are re-entrant; concurrent calls must not share a
+ *     workspace.  All kernels are compiled ahead of time for sm_103a; nothing
+ *     is compiled or loaded at run time.
+ */
+#ifndef WNA16_MOE_H
+#define WNA16_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define WNA16_API __attribute__((visibility("default")))
+#else
+#define WNA16_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WNA16_OK = 0,
+    WNA16_ERR_INVALID_ARG = -1,       /* null/misaligned pointer, bad size, overlap     */
+    WNA16_ERR_UNSUPPORTED = -2,       /* valid but not implemented (bits, group, dims)  */
+    WNA16_ERR_WORKSPACE_TOO_SMALL = -3,
+    WNA16_ERR_CUDA = -4,              /* a CUDA runtime call or launch failed            */
+    /* device status word values (wna16_moe_read_status): */
+    WNA16_ERR_BAD_ROUTING = -5,       /* an expert id was outside [0, E); its slot adds 0 */
+    WNA16_ERR_DEVICE_TIMEOUT = -6     /* a pipeline wait gave up; the output is invalid  */
+} wna16_status;
+
+/* Pack signed codes into INT32 words (page "hampsonw/DeepSeek-V4-Flash-0731-
+ * WNA16", section "How it was created", step 4).
+ *   codes   int8 device [rows, K], each in [-2^(bits-1), 2^(bits-1))
+ *   packed  int32 device [rows, K*bits/32] (written)
+ * bits in {2, 4}; K a multiple of 32/bits.  Codes outside the range are
+ * masked to their low `bits` bits after the offset is added (garbage in,
+ * garbage out; never out of bounds). */
+WNA16_API int wna16_moe_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
+                   void* stream);
+
+/* Bytes of workspace a forward with these sizes needs (0 if unsupported). */
+WNA16_API size_t wna16_moe_workspace_size(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bits);
+
+/* The routed-expert forward (the whole hot path: route/permute, gather,
+ * grouped w13 GEMM + clamped SwiGLU, grouped w2 GEMM, weighted combine).
+ *   group_size     g13, the group of w13 along K
+ *   group_size_w2  g2, the group of w2 along N (0 = same as group_size); the
+ *                  per-projection groups are the "projection-specific group
+ *                  sizes" of page "Incubate DeepSeek V4 WNA16 runtime on SM86",
+ *                  section "Validation completed"
+ *   swiglu_limit   L > 0 (may be +inf)
+ * Supported: bits in {2,4}; group sizes multiples of 64 that divide the
+ * reduction dim (K for w13, N for w2) with at most 64 groups per row;
+ * K % 256 == 0; N % 128 == 0; 1 <= topk <= E <= 1024; T*topk < 2^31.
+ * x, out, weights and scales 16-byte aligned; out must not overlap x.
+ * Returns WNA16_OK or an error (nothing launched). */
+WNA16_API int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                      const int32_t* w13_packed, const uint16_t* w13_scales,
+                      const int32_t* w2_packed, const uint16_t* w2_scales,
+                      int64_t T, int64_t K, int64_t N, int64_t E, int topk,
+                      int group_size, int group_size_w2, int bits, float swiglu_limit,
+                      void* out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronise `stream` and read the device status word of the last call that
+ * used `workspace` (WNA16_OK, WNA16_ERR_BAD_ROUTING or
+ * WNA16_ERR_DEVICE_TIMEOUT) into *device_status.  Returns WNA16_OK or
+ * WNA16_ERR_CUDA. */
+WNA16_API int wna16_moe_read_status(const void* workspace, int* device_status, void* stream);
+
+/* Message for the last host-side error on the calling thread ("" if none). */
+WNA16_API const char* wna16_moe_last_error(void);
+
+/* ---- stage entry points, for per-stage parity tests (same conventions). ---- */
+
+/* Stage 1: routing lists.  counts int32[E], offsets int32[E+1] (offsets[E] =
+ * number of valid slots), perm int32[R] (slots sorted by (expert, slot),
+ * stable), inv int32[R] (inv[perm[i]] = i; -1 for a slot with a bad id),
+ * all written into the workspace; copied to the optional outputs. */
+WNA16_API int wna16_moe_route(const int32_t* topk_ids, int64_t T, int topk, int64_t E, int64_t K, int64_t N,
+                    int bits, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stages 1-3 only: h bf16 [R, N] in permuted order (row i = slot perm[i]). */
+WNA16_API int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_packed,
+                  const uint16_t* w13_scales, int64_t T, int64_t K, int64_t N, int64_t E, int topk,
+                  int group_size, int bits, float swiglu_limit, void* h_out,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage 4 alone: y bf16 [R, K] = W2 h for permuted rows; needs the routing
+ * lists from wna16_moe_route in the same workspace and h [R, N] in permuted
+ * order. */
+WNA16_API int wna16_moe_w2(const void* h, const int32_t* w2_packed, const uint16_t* w2_scales,
+                 int64_t T, int64_t K, int64_t N, int64_t E, int topk, int group_size_w2, int bits,
+                 void* y_out, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Stage 5 alone: out bf16 [T, K] from y bf16 [R, K] (permuted order) using
+ * the inverse map of the routing lists in the workspace. */
+WNA16_API int wna16_moe_combine(const void* y, const float* topk_weights, int64_t T, int64_t K, int topk,
+                      int64_t E, int64_t N, int bits, void* out, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/* ---- instrumentation (not part of the method): per-stage device times. ----
+ * wna16_moe_profile(slots) with slots > 0 makes every later
+ * wna16_moe_forward on the calling thread record CUDA events on its stream
+ * before each of its five stages (route, gather, w13, w2, combine) and after
+ * the last, into a ring of `slots` forwards; 0 turns it off.  Forwards can be
+ * queued without waiting.  wna16_moe_profile_read(ms, n) waits for the last
+ * n recorded forwards (n <= slots) and writes their stage durations in
+ * milliseconds to ms[5*i + stage], oldest first.
+ * Both return WNA16_OK, WNA16_ERR_INVALID_ARG or WNA16_ERR_CUDA. */
+WNA16_API int wna16_moe_profile(int slots);
+WNA16_API int wna16_moe_profile_read(float* ms, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WNA16_MOE_H */

@@ -1,0 +1,114 @@
+"""C ABI checks that need no GPU: the library builds, loads, exports every
+symbol the header declares, and rejects bad arguments on the host before any
+CUDA call (so these run on a machine without a GPU)."""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import pytest
+
+from wna16_grouped_gemm_gb300 import binding, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = binding.exported_names_in_header()
+    assert len(names) == 11, names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_kernels_are_built_for_sm103a():
+    assert "arch=compute_103a,code=sm_103a" in " ".join(build.ARCH)
+
+
+# fake device pointers: never dereferenced, because validation fails first
+A16 = ctypes.c_void_p(0x10000)
+A8 = ctypes.c_void_p(0x10008)
+
+
+def _fwd(lib, *, x=A16, out=ctypes.c_void_p(0x90000), T=4, K=4096, N=2048, E=256, topk=8, g=128, g2=0, bits=2,
+         limit=7.0, ws=ctypes.c_void_p(0x100000), ws_bytes=1 << 40, ids=A16, w=A16, w13=A16, w2=A16):
+    return lib.wna16_moe_forward(x, ids, w, w13, A16, w2, A16, T, K, N, E, topk, g, g2, bits, limit, out, ws,
+                                 ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(bits=3), binding.ERR_UNSUPPORTED),
+    (dict(bits=8), binding.ERR_UNSUPPORTED),
+    (dict(K=100), binding.ERR_UNSUPPORTED),
+    (dict(N=96), binding.ERR_UNSUPPORTED),
+    (dict(g=32), binding.ERR_UNSUPPORTED),
+    (dict(g=96), binding.ERR_UNSUPPORTED),
+    (dict(g2=192), binding.ERR_UNSUPPORTED),
+    (dict(topk=9, E=8), binding.ERR_INVALID_ARG),
+    (dict(E=2048), binding.ERR_UNSUPPORTED),
+    (dict(T=-1), binding.ERR_INVALID_ARG),
+    (dict(limit=0.0), binding.ERR_INVALID_ARG),
+    (dict(limit=-1.0), binding.ERR_INVALID_ARG),
+    (dict(limit=math.nan), binding.ERR_INVALID_ARG),
+    (dict(x=None), binding.ERR_INVALID_ARG),
+    (dict(x=A8), binding.ERR_INVALID_ARG),
+    (dict(ids=None), binding.ERR_INVALID_ARG),
+    (dict(w13=A8), binding.ERR_INVALID_ARG),
+    (dict(out=ctypes.c_void_p(0x10000 + 4096)), binding.ERR_INVALID_ARG),   # overlaps x
+    (dict(ws=None), binding.ERR_INVALID_ARG),
+    (dict(ws=ctypes.c_void_p(0x100010)), binding.ERR_INVALID_ARG),          # not 256-aligned
+    (dict(ws_bytes=1024), binding.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_forward_rejects_on_host(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+    assert lib.wna16_moe_last_error().decode() != ""
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert _fwd(lib, T=0, x=None, out=None, ws=None, ids=None) == binding.OK
+
+
+def test_workspace_size(lib):
+    assert lib.wna16_moe_workspace_size(4, 4096, 2048, 256, 8, 2) > 0
+    assert lib.wna16_moe_workspace_size(4, 4096, 2048, 256, 8, 3) == 0
+    assert lib.wna16_moe_workspace_size(4, 100, 2048, 256, 8, 2) == 0
+    big = lib.wna16_moe_workspace_size(8192, 4096, 2048, 256, 8, 4)
+    # permuted x, h and y dominate: R*(K + N + K)*2 bytes
+    R = 8192 * 8
+    assert big >= R * (4096 + 2048 + 4096) * 2
+
+
+def test_pack_rejects_on_host(lib):
+    assert lib.wna16_moe_pack(A16, 4, 64, 3, A16, None) == binding.ERR_UNSUPPORTED
+    assert lib.wna16_moe_pack(A16, 4, 60, 2, A16, None) == binding.ERR_INVALID_ARG
+    assert lib.wna16_moe_pack(None, 4, 64, 2, A16, None) == binding.ERR_INVALID_ARG
+    assert lib.wna16_moe_pack(A16, 0, 64, 2, A16, None) == binding.OK
+
+
+def test_stage_entry_points_reject_on_host(lib):
+    assert lib.wna16_moe_route(A16, 4, 8, 256, 4096, 2048, 3, None, None, None, None, A16, 1 << 40,
+                               None) == binding.ERR_UNSUPPORTED
+    assert lib.wna16_moe_w13(A16, A16, A16, A16, 4, 4096, 2048, 256, 8, 32, 2, 7.0, A16, A16, 1 << 40,
+                             None) == binding.ERR_UNSUPPORTED
+    assert lib.wna16_moe_w2(A16, A16, A16, 4, 4096, 2048, 256, 8, 128, 2, A16, A16, 16, None) == \
+        binding.ERR_WORKSPACE_TOO_SMALL
+    assert lib.wna16_moe_combine(A16, A16, 4, 4096, 8, 256, 2048, 2, A16, None, 1 << 40, None) == \
+        binding.ERR_INVALID_ARG
+
+
+def test_profile_read_without_forward_is_an_error(lib):
+    assert lib.wna16_moe_profile_read(None, 1) == binding.ERR_INVALID_ARG
+    assert lib.wna16_moe_profile(-1) == binding.ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    saved = binding._lib
+    try:
+        binding._lib = None
+        with pytest.raises(RuntimeError, match="missing"):
+            binding.load_library(str(tmp_path / "nope.so"))
+    finally:
+        binding._lib = saved

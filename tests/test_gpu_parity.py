@@ -1,0 +1,247 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU oracle.
+
+Routing lists and packed words must be bit-exact; BF16 tensors must be within
+max-abs 2e-2 and relative L2 1e-3 of the oracle on the same seeded inputs.
+Full-size prefill workloads are compared on sampled tokens (the forward is
+independent per token) plus bit-exact routing at full size.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import wna16_grouped_gemm_gb300 as m
+    from wna16_grouped_gemm_gb300 import build
+    build.build()
+    m.load_library()
+    return m
+
+
+def _inputs(w: synth.Workload, seed=0):
+    return synth.make_all(w, seed)
+
+
+def _small(T=37, K=512, N=256, E=4, topk=2, bits=2, g13=128, g2=128, zipf=0.0, name="small"):
+    return synth.Workload(name, T=T, K=K, N=N, E=E, topk=topk, bits=bits, g13=g13, g2=g2,
+                          scale_lo=0.005 if bits == 2 else 0.001, scale_hi=0.02 if bits == 2 else 0.005,
+                          zipf_s=zipf)
+
+
+def _oracle_fwd(oracle, w, inp, tokens=None, intermediates=False, limit=None):
+    return oracle.forward(inp["x"], inp["ids"], inp["weights"], inp["w13_packed"], inp["w13_scales"],
+                          inp["w2_packed"], inp["w2_scales"], bits=w.bits, group_size=w.g13, group_size_w2=w.g2,
+                          swiglu_limit=w.swiglu_limit if limit is None else limit, tokens=tokens,
+                          return_intermediates=intermediates)
+
+
+def _gpu_fwd(moe, w, d, limit=None, stream=None):
+    ws = moe.alloc_workspace(w.T, w.K, w.N, w.E, w.topk, w.bits)
+    out = moe.forward(d["x"], d["topk_ids"], d["topk_weights"], d["w13_packed"], d["w13_scales"],
+                      d["w2_packed"], d["w2_scales"], bits=w.bits, group_size=w.g13, group_size_w2=w.g2,
+                      swiglu_limit=w.swiglu_limit if limit is None else limit, workspace=ws, stream=stream)
+    status = moe.read_status(ws, stream)
+    return out, status
+
+
+# ---------------------------------------------------------------- pack
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_pack_bit_exact(moe, oracle, bits):
+    rng = np.random.default_rng(1)
+    codes = synth.random_codes(rng, (300, 512), bits)
+    got = moe.pack(torch.from_numpy(codes).cuda(), bits).cpu().numpy()
+    assert np.array_equal(got, oracle.pack(codes, bits))
+
+
+# ---------------------------------------------------------------- route
+
+@pytest.mark.parametrize("T,topk,E,zipf", [(16, 2, 8, 0.0), (4, 8, 256, 0.0), (1, 8, 256, 0.0),
+                                           (2048, 8, 256, 1.1), (8192, 8, 256, 0.0), (777, 3, 5, 0.0),
+                                           (3000, 8, 1024, 0.0)])
+def test_route_bit_exact(moe, oracle, T, topk, E, zipf):
+    w = synth.Workload("r", T=T, K=256, N=128, E=E, topk=topk, bits=2, g13=128, g2=128, scale_lo=0.01,
+                       scale_hi=0.02, zipf_s=zipf)
+    ids, _ = synth.make_routing(w, seed=3)
+    counts, offsets, perm, inv = moe.route(torch.from_numpy(ids).cuda(), E, w.K, w.N, w.bits)
+    rc, ro, rp, ri = oracle.route(ids, E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    assert np.array_equal(offsets.cpu().numpy(), ro)
+    assert np.array_equal(perm.cpu().numpy(), rp)
+    assert np.array_equal(inv.cpu().numpy(), ri)
+
+
+# ---------------------------------------------------------------- stages
+
+STAGE_CASES = [
+    ("tiny_w2", None),
+    ("small_w4", _small(bits=4, g13=128, g2=128)),
+    ("small_w2_g64", _small(bits=2, g13=64, g2=64, T=53)),
+    ("small_w4_g64_w2", _small(bits=4, g13=128, g2=64, T=300, E=3)),   # prefill-sized tiles
+]
+
+
+@pytest.mark.parametrize("name,wl", STAGE_CASES, ids=[c[0] for c in STAGE_CASES])
+def test_stages_match_oracle(moe, oracle, name, wl):
+    w = wl or synth.get(name)
+    inp = _inputs(w)
+    d = gu.to_dev(inp)
+    out_ref, h_ref, y_ref = _oracle_fwd(oracle, w, inp, intermediates=True)
+    _, _, perm, inv = oracle.route(inp["ids"], w.E)
+
+    ws = moe.alloc_workspace(w.T, w.K, w.N, w.E, w.topk, w.bits)
+    h = moe.w13(d["x"], d["topk_ids"], d["w13_packed"], d["w13_scales"], bits=w.bits, group_size=w.g13,
+                swiglu_limit=w.swiglu_limit, workspace=ws)
+    assert moe.read_status(ws) == moe.OK
+    gu.assert_close(gu.host_bits(h)[inv], h_ref, f"{name} h")
+
+    # w2 alone, fed the oracle's h (permuted order)
+    y = moe.w2(gu.dev_bf16(h_ref[perm]), d["w2_packed"], d["w2_scales"], T=w.T, topk=w.topk, bits=w.bits,
+               group_size_w2=w.g2, workspace=ws)
+    assert moe.read_status(ws) == moe.OK
+    gu.assert_close(gu.host_bits(y)[inv], y_ref, f"{name} y")
+
+    # combine alone, fed the oracle's y
+    out = moe.combine(gu.dev_bf16(y_ref[perm]), d["topk_weights"], E=w.E, N=w.N, bits=w.bits, workspace=ws)
+    s = gu.assert_close(gu.host_bits(out), out_ref, f"{name} combine")
+    assert s["le1ulp"] == 1.0, s
+
+
+# ---------------------------------------------------------------- full forward
+
+FULL = ["tiny_w2", "decode_w2", "decode_w4", "decode_w4_T1"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_forward_matches_oracle(moe, oracle, name):
+    w = synth.get(name)
+    inp = _inputs(w)
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), name)
+
+
+@pytest.mark.parametrize("name", ["prefill_w2_zipf", "prefill_w4_g64"])
+def test_prefill_forward_sampled_tokens(moe, oracle, name):
+    w = synth.get(name)
+    inp = _inputs(w)
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.OK
+    rng = np.random.default_rng(123)
+    # sample tokens, including the first and last and one routed to the most popular expert
+    counts = np.bincount(inp["ids"].ravel(), minlength=w.E)
+    top_tok = int(np.nonzero((inp["ids"] == counts.argmax()).any(axis=1))[0][-1])
+    toks = np.unique(np.concatenate([[0, w.T - 1, top_tok], rng.choice(w.T, 5, replace=False)]))
+    ref = _oracle_fwd(oracle, w, inp, tokens=toks)
+    gu.assert_close(gu.host_bits(out)[toks], ref, f"{name} sampled")
+    assert torch.isfinite(out.float()).all()
+
+
+# ---------------------------------------------------------------- edge cases
+
+def test_tile_boundaries(moe, oracle):
+    """Experts with 1, 15, 16, 17, 127, 128, 129 and 257 rows (prefill tile 128)."""
+    counts = [1, 15, 16, 17, 127, 128, 129, 257]
+    w = _small(T=sum(counts), E=len(counts), topk=1, bits=4, g13=128, g2=128)
+    inp = _inputs(w)
+    ids = np.concatenate([np.full(c, e, np.int32) for e, c in enumerate(counts)])
+    np.random.default_rng(0).shuffle(ids)
+    inp["ids"] = ids.reshape(-1, 1)
+    inp["weights"] = np.ones((w.T, 1), np.float32)
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), "tile boundaries")
+
+
+def test_small_tiles_ragged(moe, oracle):
+    """Decode-sized tiles (16 rows) with experts of 1..40 rows."""
+    w = _small(T=70, E=16, topk=3, bits=2)
+    inp = _inputs(w)
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), "ragged")
+
+
+def test_single_expert_top1(moe, oracle):
+    w = _small(T=1, E=1, topk=1, bits=4)
+    inp = _inputs(w)
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), "E=1")
+
+
+def test_duplicate_ids_in_a_row(moe, oracle):
+    w = _small(T=9, E=4, topk=3, bits=2)
+    inp = _inputs(w)
+    inp["ids"][:, 1] = inp["ids"][:, 0]
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), "duplicates")
+
+
+def test_bad_expert_id_sets_status_and_adds_zero(moe, oracle):
+    w = _small(T=10, E=4, topk=2, bits=2)
+    inp = _inputs(w)
+    inp["ids"][3, 1] = 7
+    inp["ids"][5, 0] = -1
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.ERR_BAD_ROUTING
+    ref_inp = dict(inp, ids=inp["ids"].copy(), weights=inp["weights"].copy())
+    for t, j in ((3, 1), (5, 0)):
+        ref_inp["ids"][t, j] = 0
+        ref_inp["weights"][t, j] = 0.0
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, ref_inp), "bad ids")
+
+
+def test_no_clamp_limit_inf(moe, oracle):
+    w = _small(T=12, E=4, topk=2, bits=4)
+    inp = _inputs(w)
+    # large scales so that some gate/up values pass the 7.0 limit
+    inp["w13_scales"] = (inp["w13_scales"].astype(np.float32) * 40).astype(np.float16)
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp), limit=float("inf"))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp, limit=float("inf")), "limit inf")
+    out7, _ = _gpu_fwd(moe, w, gu.to_dev(inp), limit=7.0)
+    gu.assert_close(gu.host_bits(out7), _oracle_fwd(oracle, w, inp, limit=7.0), "limit 7 large")
+
+
+def test_empty_batch(moe):
+    w = _small(T=0, E=4, topk=2)
+    d = gu.to_dev(_inputs(_small(T=1, E=4, topk=2)))
+    x = d["x"][:0]
+    ids = d["topk_ids"][:0]
+    wt = d["topk_weights"][:0]
+    out = moe.forward(x, ids, wt, d["w13_packed"], d["w13_scales"], d["w2_packed"], d["w2_scales"], bits=w.bits,
+                      group_size=w.g13, workspace=torch.empty(256, dtype=torch.uint8, device="cuda"))
+    assert out.shape == (0, w.K)
+
+
+def test_deterministic_and_stream(moe):
+    w = synth.get("decode_w4")
+    d = gu.to_dev(_inputs(w))
+    a, _ = _gpu_fwd(moe, w, d)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        b, st = _gpu_fwd(moe, w, d, stream=s)
+    s.synchronize()
+    assert st == moe.OK
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_scale_doubling_is_exact_on_gpu(moe):
+    """Doubling every w2 scale doubles the output bit-exactly (also true of the oracle)."""
+    w = _small(T=20, E=4, topk=2, bits=4)
+    inp = _inputs(w)
+    d = gu.to_dev(inp)
+    a, _ = _gpu_fwd(moe, w, d)
+    d2 = dict(d, w2_scales=(d["w2_scales"].float() * 2).half())
+    b, _ = _gpu_fwd(moe, w, d2)
+    assert torch.equal(b.float(), 2 * a.float())

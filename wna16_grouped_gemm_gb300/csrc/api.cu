@@ -1,0 +1,527 @@
+// C ABI of the WNA16 routed-expert MoE forward: argument validation,
+// workspace layout, TMA descriptors and the launch sequence
+//   route -> gather -> grouped w13 (+SwiGLU) -> grouped w2 -> combine
+// on the caller's stream.  See include/wna16_moe.h for the contract.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/wna16_moe.h"
+#include "gemm.h"
+
+using namespace wna16;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+// Per-thread stage events for wna16_moe_profile (instrumentation only): a
+// ring of `slots` forwards x 6 events, so that a caller can queue many
+// forwards without waiting and read all their stage times afterwards.
+struct StageEvents {
+    int slots = 0;          // 0: off
+    int next = 0;           // ring position of the next forward
+    long long recorded = 0; // forwards recorded since enabled
+    cudaEvent_t* ev = nullptr;
+};
+thread_local StageEvents g_prof;
+
+inline void mark(int i, cudaStream_t s) {
+    if (g_prof.slots) cudaEventRecord(g_prof.ev[g_prof.next * 6 + i], s);
+}
+inline void mark_done() {
+    if (g_prof.slots) {
+        g_prof.next = (g_prof.next + 1) % g_prof.slots;
+        ++g_prof.recorded;
+    }
+}
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(WNA16_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+
+// Token tile (MMA N) from the mean rows per expert.
+int choose_nt(int64_t R, int64_t E) {
+    const double avg = static_cast<double>(R) / static_cast<double>(E);
+    if (avg <= 4.0) return 16;
+    if (avg <= 16.0) return 32;
+    if (avg <= 48.0) return 64;
+    return 128;
+}
+
+struct Layout {
+    int64_t R = 0;
+    int nt = 16;
+    int64_t max_tiles = 0;
+    size_t status = 0, n_tiles = 0, counts = 0, offsets = 0, perm = 0, inv = 0, tiles = 0, xp = 0, h = 0, y = 0;
+    size_t total = 0;
+};
+
+Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk) {
+    Layout L;
+    L.R = T * topk;
+    L.nt = choose_nt(L.R, E);
+    L.max_tiles = (L.R < E ? L.R : E) + L.R / L.nt + 1;
+    size_t o = 0;
+    L.status = o;   o = align_up(o + sizeof(int));
+    L.n_tiles = o;  o = align_up(o + sizeof(int));
+    L.counts = o;   o = align_up(o + sizeof(int) * E);
+    L.offsets = o;  o = align_up(o + sizeof(int) * (E + 1));
+    L.perm = o;     o = align_up(o + sizeof(int) * L.R);
+    L.inv = o;      o = align_up(o + sizeof(int) * L.R);
+    L.tiles = o;    o = align_up(o + sizeof(int4) * L.max_tiles);
+    L.xp = o;       o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
+    L.h = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * N);
+    L.y = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
+    L.total = o;
+    return L;
+}
+
+template <typename P>
+P* at(void* ws, size_t off) {
+    return reinterpret_cast<P*>(static_cast<char*>(ws) + off);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------- device info
+
+struct DevInfo {
+    int sms = 0;
+    int max_smem = 0;
+};
+
+int device_info(DevInfo& d) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    static std::mutex mu;
+    static DevInfo cache[64];
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && cache[dev].sms) {
+        d = cache[dev];
+        return WNA16_OK;
+    }
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+        return fail(WNA16_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, major,
+                    minor);
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (dev < 64) cache[dev] = d;
+    return WNA16_OK;
+}
+
+// ---------------------------------------------------------------- TMA descriptors
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor [rows, cols] of `elem`-byte elements, box [box_rows, box_cols].
+int encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem, const void* base, uint64_t rows,
+              uint64_t cols, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(WNA16_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem)};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(WNA16_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return WNA16_OK;
+}
+
+CUtensorMapSwizzle swizzle_for_pitch(int pitch) {
+    switch (pitch) {
+        case 32: return CU_TENSOR_MAP_SWIZZLE_32B;
+        case 64: return CU_TENSOR_MAP_SWIZZLE_64B;
+        case 128: return CU_TENSOR_MAP_SWIZZLE_128B;
+        default: return CU_TENSOR_MAP_SWIZZLE_NONE;
+    }
+}
+
+// ---------------------------------------------------------------- validation
+
+int check_dims(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bits) {
+    if (T < 0 || K <= 0 || N <= 0 || E <= 0 || topk <= 0)
+        return fail(WNA16_ERR_INVALID_ARG, "sizes must be positive (T may be 0): T=%lld K=%lld N=%lld E=%lld topk=%d",
+                    (long long)T, (long long)K, (long long)N, (long long)E, topk);
+    if (bits != 2 && bits != 4) return fail(WNA16_ERR_UNSUPPORTED, "bits=%d: only 2 and 4 are supported", bits);
+    if (topk > E) return fail(WNA16_ERR_INVALID_ARG, "topk=%d exceeds E=%lld", topk, (long long)E);
+    if (E > 1024) return fail(WNA16_ERR_UNSUPPORTED, "E=%lld: at most 1024 experts", (long long)E);
+    if (K % 256) return fail(WNA16_ERR_UNSUPPORTED, "K=%lld must be a multiple of 256", (long long)K);
+    if (N % 128) return fail(WNA16_ERR_UNSUPPORTED, "N=%lld must be a multiple of 128", (long long)N);
+    if (T * topk >= (int64_t(1) << 31)) return fail(WNA16_ERR_UNSUPPORTED, "T*topk must be < 2^31");
+    if (E * 2 * N >= (int64_t(1) << 31) || E * K >= (int64_t(1) << 31))
+        return fail(WNA16_ERR_UNSUPPORTED, "E*2N and E*K must be < 2^31 weight rows");
+    return WNA16_OK;
+}
+
+int check_group(int g, int64_t kred, const char* name) {
+    if (g <= 0 || g % 64 || kred % g)
+        return fail(WNA16_ERR_UNSUPPORTED, "%s=%d: groups must be multiples of 64 that divide %lld", name, g,
+                    (long long)kred);
+    if (kred / g > 64) return fail(WNA16_ERR_UNSUPPORTED, "%s=%d: at most 64 groups per row", name, g);
+    return WNA16_OK;
+}
+
+int check_ptr(const void* p, size_t align, const char* name) {
+    if (!p) return fail(WNA16_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, align)) return fail(WNA16_ERR_INVALID_ARG, "%s must be %zu-byte aligned", name, align);
+    return WNA16_OK;
+}
+
+int check_workspace(const void* ws, size_t bytes, const Layout& L) {
+    if (int rc = check_ptr(ws, kAlign, "workspace")) return rc;
+    if (bytes < L.total)
+        return fail(WNA16_ERR_WORKSPACE_TOO_SMALL, "workspace has %zu bytes, needs %zu", bytes, L.total);
+    return WNA16_OK;
+}
+
+// ---------------------------------------------------------------- launch helpers
+
+int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStream_t s) {
+    cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), L.nt, at<int>(ws, L.counts),
+                                 at<int>(ws, L.offsets), at<int>(ws, L.perm), at<int>(ws, L.inv),
+                                 at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status), s);
+    return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "route kernel launch");
+}
+
+// One grouped GEMM, prepared on the host (tensor maps, parameters, launch
+// shape) before anything is launched: w13 (B = Xp [R, K], out = h [R, N]) or
+// w2 (B = h [R, N], out = y [R, K]).
+struct GemmPlan {
+    bool w13 = true;
+    int bits = 2;
+    CUtensorMap tm_w, tm_b;
+    GemmParams gp{};
+    int grid = 0;
+    int smem = 0;
+};
+
+int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uint16_t* wscales, const void* b_src,
+              void* out, int64_t K, int64_t N, int64_t E, int group, float limit, const Layout& L, void* ws) {
+    DevInfo dev;
+    if (int rc = device_info(dev)) return rc;
+    const int64_t kred = w13 ? K : N;
+    const int64_t rows_per_expert = w13 ? 2 * N : K;
+    const int nt = L.nt;
+    int kp;
+    if (nt <= 32) {
+        kp = 1024 / bits;                       // 128 packed bytes per row per stage
+        while (kred % kp) kp /= 2;
+    } else {
+        kp = 64;
+    }
+    const int pitch = kp * bits / 8;
+    const int ngroups = static_cast<int>(kred / group);
+    GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups, dev.max_smem);
+    if (sm.nstage < 2) return fail(WNA16_ERR_UNSUPPORTED, "shared-memory plan does not fit");
+
+    const int p = 32 / bits;
+    if (int rc = encode_2d(&P.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, wpacked,
+                           static_cast<uint64_t>(E * rows_per_expert), static_cast<uint64_t>(kred / p), 128,
+                           static_cast<uint32_t>(pitch / 4), swizzle_for_pitch(pitch)))
+        return rc;
+    if (int rc = encode_2d(&P.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b_src, static_cast<uint64_t>(L.R),
+                           static_cast<uint64_t>(kred), static_cast<uint32_t>(nt), 64, CU_TENSOR_MAP_SWIZZLE_128B))
+        return rc;
+
+    GemmParams& gp = P.gp;
+    gp.tiles = at<const int4>(ws, L.tiles);
+    gp.n_tiles = at<const int>(ws, L.n_tiles);
+    gp.scales = wscales;
+    gp.out = static_cast<__nv_bfloat16*>(out);
+    gp.out_ld = static_cast<int>(w13 ? N : K);
+    gp.rows_per_expert = static_cast<int>(rows_per_expert);
+    gp.half_rows = static_cast<int>(N);
+    gp.kred = static_cast<int>(kred);
+    gp.ngroups = ngroups;
+    gp.group = group;
+    gp.mt_count = static_cast<int>(w13 ? N / 128 : K / 256);
+    gp.kp = kp;
+    gp.nt = nt;
+    gp.nstage = sm.nstage;
+    gp.off_b = sm.off_b;
+    gp.off_w = sm.off_w;
+    gp.off_s = sm.off_s;
+    gp.off_bar = sm.off_bar;
+    gp.limit = limit;
+    gp.status = at<int>(ws, L.status);
+
+    const int64_t max_units = L.max_tiles * gp.mt_count;
+    P.grid = static_cast<int>(max_units < dev.sms ? max_units : dev.sms);
+    P.smem = sm.total;
+    P.w13 = w13;
+    P.bits = bits;
+    return WNA16_OK;
+}
+
+int launch_plan(const GemmPlan& P, cudaStream_t s) {
+    cudaError_t e = launch_grouped_gemm(P.bits, P.w13, P.tm_w, P.tm_b, P.gp, P.grid, P.smem, s);
+    return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "grouped GEMM launch");
+}
+
+}  // namespace
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* wna16_moe_last_error(void) { return g_err; }
+
+size_t wna16_moe_workspace_size(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bits) {
+    if (check_dims(T, K, N, E, topk, bits) != WNA16_OK) return 0;
+    return make_layout(T, K, N, E, topk).total;
+}
+
+int wna16_moe_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed, void* stream) {
+    g_err[0] = 0;
+    if (bits != 2 && bits != 4) return fail(WNA16_ERR_UNSUPPORTED, "bits=%d: only 2 and 4 are supported", bits);
+    if (rows < 0 || K <= 0 || K % (32 / bits))
+        return fail(WNA16_ERR_INVALID_ARG, "K=%lld must be a positive multiple of %d", (long long)K, 32 / bits);
+    if (rows == 0) return WNA16_OK;
+    if (int rc = check_ptr(codes, 1, "codes")) return rc;
+    if (int rc = check_ptr(packed, 4, "packed")) return rc;
+    cudaError_t e = launch_pack(codes, rows, K, bits, packed, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "pack kernel launch");
+}
+
+int wna16_moe_read_status(const void* workspace, int* device_status, void* stream) {
+    g_err[0] = 0;
+    if (!workspace || !device_status) return fail(WNA16_ERR_INVALID_ARG, "NULL argument");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    e = cudaMemcpy(device_status, workspace, sizeof(int), cudaMemcpyDeviceToHost);  // status is at offset 0
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+    return WNA16_OK;
+}
+
+int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_weights, const int32_t* w13_packed,
+                      const uint16_t* w13_scales, const int32_t* w2_packed, const uint16_t* w2_scales, int64_t T,
+                      int64_t K, int64_t N, int64_t E, int topk, int group_size, int group_size_w2, int bits,
+                      float swiglu_limit, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    if (int rc = check_dims(T, K, N, E, topk, bits)) return rc;
+    const int g2 = group_size_w2 ? group_size_w2 : group_size;
+    if (int rc = check_group(group_size, K, "group_size")) return rc;
+    if (int rc = check_group(g2, N, "group_size_w2")) return rc;
+    if (!(swiglu_limit > 0.0f)) return fail(WNA16_ERR_INVALID_ARG, "swiglu_limit must be > 0 (or +inf)");
+    if (T == 0) return WNA16_OK;
+    if (int rc = check_ptr(x, 16, "x")) return rc;
+    if (int rc = check_ptr(out, 16, "out")) return rc;
+    if (int rc = check_ptr(topk_ids, 4, "topk_ids")) return rc;
+    if (int rc = check_ptr(topk_weights, 4, "topk_weights")) return rc;
+    if (int rc = check_ptr(w13_packed, 16, "w13_packed")) return rc;
+    if (int rc = check_ptr(w2_packed, 16, "w2_packed")) return rc;
+    if (int rc = check_ptr(w13_scales, 2, "w13_scales")) return rc;
+    if (int rc = check_ptr(w2_scales, 2, "w2_scales")) return rc;
+    {
+        const uintptr_t xb = reinterpret_cast<uintptr_t>(x), ob = reinterpret_cast<uintptr_t>(out);
+        const uintptr_t bytes = static_cast<uintptr_t>(T * K * 2);
+        if (xb < ob + bytes && ob < xb + bytes) return fail(WNA16_ERR_INVALID_ARG, "out overlaps x");
+    }
+    const Layout L = make_layout(T, K, N, E, topk);
+    if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmPlan p13, p2;
+    if (int rc = plan_gemm(p13, true, bits, w13_packed, w13_scales, at<void>(workspace, L.xp),
+                           at<void>(workspace, L.h), K, N, E, group_size, swiglu_limit, L, workspace))
+        return rc;
+    if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, at<void>(workspace, L.h), at<void>(workspace, L.y),
+                           K, N, E, g2, swiglu_limit, L, workspace))
+        return rc;
+
+    mark(0, s);
+    if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
+    mark(1, s);
+    cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
+                                  at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
+                                  static_cast<int>(K), at<__nv_bfloat16>(workspace, L.xp), s);
+    if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+    mark(2, s);
+    if (int rc = launch_plan(p13, s)) return rc;
+    mark(3, s);
+    if (int rc = launch_plan(p2, s)) return rc;
+    mark(4, s);
+    e = launch_combine(at<__nv_bfloat16>(workspace, L.y), topk_weights, at<int>(workspace, L.inv),
+                       static_cast<int>(T), topk, static_cast<int>(K), static_cast<__nv_bfloat16*>(out), s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
+    mark(5, s);
+    mark_done();
+    return WNA16_OK;
+}
+
+int wna16_moe_profile(int slots) {
+    g_err[0] = 0;
+    if (slots < 0 || slots > 65536) return fail(WNA16_ERR_INVALID_ARG, "slots=%d must be in [0, 65536]", slots);
+    if (g_prof.ev) {
+        for (int i = 0; i < g_prof.slots * 6; ++i) cudaEventDestroy(g_prof.ev[i]);
+        delete[] g_prof.ev;
+        g_prof.ev = nullptr;
+    }
+    g_prof.slots = 0;
+    g_prof.next = 0;
+    g_prof.recorded = 0;
+    if (slots == 0) return WNA16_OK;
+    g_prof.ev = new cudaEvent_t[static_cast<size_t>(slots) * 6];
+    for (int i = 0; i < slots * 6; ++i) {
+        cudaError_t e = cudaEventCreate(&g_prof.ev[i]);
+        if (e != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
+            delete[] g_prof.ev;
+            g_prof.ev = nullptr;
+            return cuda_fail(e, "cudaEventCreate");
+        }
+    }
+    g_prof.slots = slots;
+    return WNA16_OK;
+}
+
+int wna16_moe_profile_read(float* ms, int n) {
+    g_err[0] = 0;
+    if (!ms || n <= 0) return fail(WNA16_ERR_INVALID_ARG, "ms is NULL or n <= 0");
+    if (!g_prof.slots || n > g_prof.slots || n > g_prof.recorded)
+        return fail(WNA16_ERR_INVALID_ARG, "only %lld profiled forwards available (ring of %d)", g_prof.recorded,
+                    g_prof.slots);
+    for (int f = 0; f < n; ++f) {
+        const int slot = ((g_prof.next - n + f) % g_prof.slots + g_prof.slots) % g_prof.slots;
+        cudaEvent_t* ev = g_prof.ev + slot * 6;
+        cudaError_t e = cudaEventSynchronize(ev[5]);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+        for (int i = 0; i < 5; ++i) {
+            e = cudaEventElapsedTime(&ms[f * 5 + i], ev[i], ev[i + 1]);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+        }
+    }
+    return WNA16_OK;
+}
+
+int wna16_moe_route(const int32_t* topk_ids, int64_t T, int topk, int64_t E, int64_t K, int64_t N, int bits,
+                    int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    if (int rc = check_dims(T, K, N, E, topk, bits)) return rc;
+    const Layout L = make_layout(T, K, N, E, topk);
+    if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
+    if (T > 0)
+        if (int rc = check_ptr(topk_ids, 4, "topk_ids")) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
+    struct {
+        void* dst;
+        size_t off, bytes;
+    } copies[4] = {{counts, L.counts, sizeof(int) * E},
+                   {offsets, L.offsets, sizeof(int) * (E + 1)},
+                   {perm, L.perm, sizeof(int) * L.R},
+                   {inv, L.inv, sizeof(int) * L.R}};
+    for (auto& c : copies) {
+        if (!c.dst || c.bytes == 0) continue;
+        cudaError_t e = cudaMemcpyAsync(c.dst, at<char>(workspace, c.off), c.bytes, cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+    }
+    return WNA16_OK;
+}
+
+int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_packed, const uint16_t* w13_scales,
+                  int64_t T, int64_t K, int64_t N, int64_t E, int topk, int group_size, int bits, float swiglu_limit,
+                  void* h_out, void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    if (int rc = check_dims(T, K, N, E, topk, bits)) return rc;
+    if (int rc = check_group(group_size, K, "group_size")) return rc;
+    if (!(swiglu_limit > 0.0f)) return fail(WNA16_ERR_INVALID_ARG, "swiglu_limit must be > 0 (or +inf)");
+    if (T == 0) return WNA16_OK;
+    if (int rc = check_ptr(x, 16, "x")) return rc;
+    if (int rc = check_ptr(h_out, 16, "h_out")) return rc;
+    if (int rc = check_ptr(topk_ids, 4, "topk_ids")) return rc;
+    if (int rc = check_ptr(w13_packed, 16, "w13_packed")) return rc;
+    if (int rc = check_ptr(w13_scales, 2, "w13_scales")) return rc;
+    const Layout L = make_layout(T, K, N, E, topk);
+    if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    GemmPlan p13;
+    if (int rc = plan_gemm(p13, true, bits, w13_packed, w13_scales, at<void>(workspace, L.xp), h_out, K, N, E,
+                           group_size, swiglu_limit, L, workspace))
+        return rc;
+    if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
+    cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
+                                  at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
+                                  static_cast<int>(K), at<__nv_bfloat16>(workspace, L.xp), s);
+    if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+    return launch_plan(p13, s);
+}
+
+int wna16_moe_w2(const void* h, const int32_t* w2_packed, const uint16_t* w2_scales, int64_t T, int64_t K, int64_t N,
+                 int64_t E, int topk, int group_size_w2, int bits, void* y_out, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    if (int rc = check_dims(T, K, N, E, topk, bits)) return rc;
+    if (int rc = check_group(group_size_w2, N, "group_size_w2")) return rc;
+    if (T == 0) return WNA16_OK;
+    if (int rc = check_ptr(h, 16, "h")) return rc;
+    if (int rc = check_ptr(y_out, 16, "y_out")) return rc;
+    if (int rc = check_ptr(w2_packed, 16, "w2_packed")) return rc;
+    if (int rc = check_ptr(w2_scales, 2, "w2_scales")) return rc;
+    const Layout L = make_layout(T, K, N, E, topk);
+    if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
+    GemmPlan p2;
+    if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, h, y_out, K, N, E, group_size_w2, INFINITY, L,
+                           workspace))
+        return rc;
+    return launch_plan(p2, static_cast<cudaStream_t>(stream));
+}
+
+int wna16_moe_combine(const void* y, const float* topk_weights, int64_t T, int64_t K, int topk, int64_t E, int64_t N,
+                      int bits, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    g_err[0] = 0;
+    if (int rc = check_dims(T, K, N, E, topk, bits)) return rc;
+    if (T == 0) return WNA16_OK;
+    if (int rc = check_ptr(y, 16, "y")) return rc;
+    if (int rc = check_ptr(out, 16, "out")) return rc;
+    if (int rc = check_ptr(topk_weights, 4, "topk_weights")) return rc;
+    const Layout L = make_layout(T, K, N, E, topk);
+    if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
+    cudaError_t e = launch_combine(static_cast<const __nv_bfloat16*>(y), topk_weights, at<int>(workspace, L.inv),
+                                   static_cast<int>(T), topk, static_cast<int>(K), static_cast<__nv_bfloat16*>(out),
+                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "combine kernel launch");
+}
+
+}  // extern "C"

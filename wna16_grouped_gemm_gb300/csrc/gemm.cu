@@ -1,0 +1,503 @@
+// Grouped WNA16 expert GEMM for sm_103a (tcgen05 + TMEM + TMA), used for both
+// projections of the routed-expert MoE ("Incubate DeepSeek V4 WNA16 runtime on
+// SM86", section "What this branch adds", items 1-3 and 9):
+//
+//   w13 unit:  D_gate[n, t] = sum_k W1_e[n, k] X[t, k],  D_up likewise with W3_e
+//              h[t, n]      = bf16( silu(min(D_gate, L)) * clamp(D_up, -L, L) )
+//   w2  unit:  y[t, m]      = bf16( sum_n W2_e[m, n] H[t, n] )
+//
+// The weights are the M side of the MMA ("swap AB"): a unit is 2 x 128 weight
+// rows (gate+up rows n0.., or 256 consecutive w2 rows) against one token tile
+// of up to NT rows of a single expert.  Per K step:
+//
+//   TMA producer (warp 0)   packed INT32 tiles of both weight row blocks and the
+//                           token tile (128B-swizzled BF16) -> smem stage ring
+//   scale loader (warp 2)   the unit's FP16 scales -> smem (transposed)
+//   dequant warps (4..11)   each thread owns one weight row: reads its packed
+//                           words, builds bf16(code*scale) exactly, and writes
+//                           them into a TMEM A buffer with tcgen05.st
+//   MMA issuer (warp 1)     tcgen05.mma kind::f16, A from TMEM, B from smem,
+//                           fp32 accumulators in TMEM (one per row block)
+//   epilogue (warps 4..11)  tcgen05.ld accumulators -> SwiGLU / plain -> BF16
+//
+// Keeping the dequantised A operand in TMEM means shared memory only carries
+// the packed words and the token tile: the BF16 weights never cross the
+// shared-memory port, which would otherwise cap decode far below HBM speed.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "gemm.h"
+#include "ptx.cuh"
+
+namespace wna16 {
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr int kRowsPerTile = 128;
+constexpr int kKA = 64;          // K elements per TMEM A buffer (per row block)
+constexpr int kNumABuf = 4;      // TMEM A ring
+constexpr int kTmemCols = 512;
+
+struct Ring {
+    uint32_t idx = 0, phase = 0;
+    __device__ __forceinline__ void next(uint32_t n) {
+        if (++idx == n) {
+            idx = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// ------------------------------------------------------------------ dequant
+//
+// A b-bit field q placed at mantissa bit `pos` of a float whose exponent
+// field is (150 - pos) reads as 2^(23-pos) + q.  fma(that, s, -(2^(23-pos) +
+// 2^(b-1)) * s) then equals (q - 2^(b-1)) * s = code * s EXACTLY: the product
+// has at most 4 + 11 significant bits and the offset constant at most 13 + 11
+// <= 24 bits for the positions used (10..20 for 2-bit, 8..16 for 4-bit
+// fields), so the single rounding of the FMA has nothing to round.  One
+// cvt.rn.bf16x2 then gives the correctly rounded BF16 weights.
+template <int POS>
+__device__ __forceinline__ uint32_t magic_bits() {
+    return static_cast<uint32_t>(150 - POS) << 23;
+}
+
+template <int BITS, int POS>
+__device__ __forceinline__ float field_value(uint32_t src, float s, float negoff) {
+    constexpr uint32_t mask = ((1u << BITS) - 1u) << POS;
+    const uint32_t b = (src & mask) | magic_bits<POS>();
+    return __fmaf_rn(__uint_as_float(b), s, negoff);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Constants -(2^(23-pos) + 2^(b-1)) * s for one scale.
+struct Neg2 {  // 2-bit: pos 10, 12, 14, 16, 18, 20
+    float c10, c12, c14, c16, c18, c20;
+    __device__ __forceinline__ explicit Neg2(float s)
+        : c10(-8194.0f * s), c12(-2050.0f * s), c14(-514.0f * s), c16(-130.0f * s), c18(-34.0f * s),
+          c20(-10.0f * s) {}
+};
+struct Neg4 {  // 4-bit: pos 8, 12, 16
+    float c8, c12, c16;
+    __device__ __forceinline__ explicit Neg4(float s) : c8(-32776.0f * s), c12(-2056.0f * s), c16(-136.0f * s) {}
+};
+
+// One 2-bit word (16 consecutive k) -> 8 bf16x2 (pairs k, k+1).
+__device__ __forceinline__ void dequant_word2(uint32_t w, float s, const Neg2& c, uint32_t* o) {
+    const uint32_t a = w << 12;   // fields 0..4 at bits 12..20
+    const uint32_t m = w;         // fields 5..10 at bits 10..20
+    const uint32_t r = w >> 12;   // fields 11..15 at bits 10..18
+    o[0] = pack_bf16x2(field_value<2, 12>(a, s, c.c12), field_value<2, 14>(a, s, c.c14));
+    o[1] = pack_bf16x2(field_value<2, 16>(a, s, c.c16), field_value<2, 18>(a, s, c.c18));
+    o[2] = pack_bf16x2(field_value<2, 20>(a, s, c.c20), field_value<2, 10>(m, s, c.c10));
+    o[3] = pack_bf16x2(field_value<2, 12>(m, s, c.c12), field_value<2, 14>(m, s, c.c14));
+    o[4] = pack_bf16x2(field_value<2, 16>(m, s, c.c16), field_value<2, 18>(m, s, c.c18));
+    o[5] = pack_bf16x2(field_value<2, 20>(m, s, c.c20), field_value<2, 10>(r, s, c.c10));
+    o[6] = pack_bf16x2(field_value<2, 12>(r, s, c.c12), field_value<2, 14>(r, s, c.c14));
+    o[7] = pack_bf16x2(field_value<2, 16>(r, s, c.c16), field_value<2, 18>(r, s, c.c18));
+}
+
+// One 4-bit word (8 consecutive k) -> 4 bf16x2.
+__device__ __forceinline__ void dequant_word4(uint32_t w, float s, const Neg4& c, uint32_t* o) {
+    const uint32_t a = w << 8;    // nibbles 0, 1 at bits 8, 12
+    const uint32_t m = w;         // nibbles 2, 3, 4 at bits 8, 12, 16
+    const uint32_t r = w >> 12;   // nibbles 5, 6, 7 at bits 8, 12, 16
+    o[0] = pack_bf16x2(field_value<4, 8>(a, s, c.c8), field_value<4, 12>(a, s, c.c12));
+    o[1] = pack_bf16x2(field_value<4, 8>(m, s, c.c8), field_value<4, 12>(m, s, c.c12));
+    o[2] = pack_bf16x2(field_value<4, 16>(m, s, c.c16), field_value<4, 8>(r, s, c.c8));
+    o[3] = pack_bf16x2(field_value<4, 12>(r, s, c.c12), field_value<4, 16>(r, s, c.c16));
+}
+
+// 64 consecutive k of one row (one TMEM A buffer row) -> 32 bf16x2.
+// `row` = this row's packed bytes in the stage, `xr` = its swizzle XOR,
+// `chunk` = which 64-k chunk of the stage.
+template <int BITS>
+__device__ __forceinline__ void dequant_chunk(const uint8_t* row, uint32_t xr, int chunk, float s,
+                                              uint32_t (&o)[32]) {
+    if constexpr (BITS == 2) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((static_cast<uint32_t>(chunk) ^ xr) << 4));
+        const Neg2 c(s);
+        dequant_word2(v.x, s, c, o + 0);
+        dequant_word2(v.y, s, c, o + 8);
+        dequant_word2(v.z, s, c, o + 16);
+        dequant_word2(v.w, s, c, o + 24);
+    } else {
+        const uint32_t j0 = static_cast<uint32_t>(2 * chunk);
+        const uint4 v0 = *reinterpret_cast<const uint4*>(row + ((j0 ^ xr) << 4));
+        const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((j0 + 1) ^ xr) << 4));
+        const Neg4 c(s);
+        dequant_word4(v0.x, s, c, o + 0);
+        dequant_word4(v0.y, s, c, o + 4);
+        dequant_word4(v0.z, s, c, o + 8);
+        dequant_word4(v0.w, s, c, o + 12);
+        dequant_word4(v1.x, s, c, o + 16);
+        dequant_word4(v1.y, s, c, o + 20);
+        dequant_word4(v1.z, s, c, o + 24);
+        dequant_word4(v1.w, s, c, o + 28);
+    }
+}
+
+__device__ __forceinline__ float swiglu(float g, float u, float L) {
+    g = fminf(g, L);
+    u = fminf(fmaxf(u, -L), L);
+    return g / (1.0f + expf(-g)) * u;
+}
+
+// Weight rows of the two 128-row blocks of unit (expert e, row tile mt).
+template <bool W13>
+__device__ __forceinline__ void unit_rows(const GemmParams& p, int e, int mt, int& r0, int& r1) {
+    const int base = e * p.rows_per_expert;
+    if constexpr (W13) {
+        r0 = base + mt * kRowsPerTile;                  // gate rows
+        r1 = base + p.half_rows + mt * kRowsPerTile;    // up rows
+    } else {
+        r0 = base + mt * 2 * kRowsPerTile;
+        r1 = r0 + kRowsPerTile;
+    }
+}
+
+}  // namespace
+
+template <int BITS, bool W13>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
+                        const GemmParams p) {
+    constexpr int kCodes = 32 / BITS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nt = p.nt;
+    const int kp = p.kp;
+    const int nstage = p.nstage;
+    const int pitch = kp * BITS / 8;                     // packed bytes per row per stage
+    const int b_stage_bytes = (kp / 64) * nt * 128;
+    const int w_tile_bytes = kRowsPerTile * pitch;
+    const int ksteps = p.kred / kp;
+    const int chunks = kp / kKA;
+
+    uint8_t* sB = smem + p.off_b;
+    uint8_t* sW = smem + p.off_w;
+    uint16_t* sS = reinterpret_cast<uint16_t*>(smem + p.off_s);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+    uint64_t* full = bars;
+    uint64_t* empty = full + nstage;
+    uint64_t* afull = empty + nstage;
+    uint64_t* aempty = afull + kNumABuf;
+    uint64_t* accfull = aempty + kNumABuf;
+    uint64_t* accempty = accfull + 1;
+    uint64_t* sfull = accempty + 1;
+    uint64_t* sempty = sfull + 2;
+    uint64_t* drain = sempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < nstage; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 8 + 1);
+        }
+        for (int i = 0; i < kNumABuf; ++i) {
+            mbar_init(&afull[i], 8);
+            mbar_init(&aempty[i], 1);
+        }
+        mbar_init(accfull, 1);
+        mbar_init(accempty, 8);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sfull[i], 32);
+            mbar_init(&sempty[i], 8);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tm_w);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int n_units = (*p.n_tiles) * p.mt_count;
+    int* status = p.status;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_b = policy_evict_last();
+            const uint32_t tx = static_cast<uint32_t>(2 * w_tile_bytes + b_stage_bytes);
+            Ring st;
+            uint32_t issued = 0, last_parity = 0;   // per slot: issued at least once / parity of last issue
+            bool ok = true;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                const int4 tile = p.tiles[u / p.mt_count];
+                int r0, r1;
+                unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (!mbar_wait_bounded(&empty[st.idx], st.phase ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st.idx], tx);
+                    uint8_t* w = sW + st.idx * 2 * w_tile_bytes;
+                    const int wc = ks * (kp / kCodes);
+                    tma_load_2d(w, &tm_w, &full[st.idx], wc, r0, pol_w);
+                    tma_load_2d(w + w_tile_bytes, &tm_w, &full[st.idx], wc, r1, pol_w);
+                    uint8_t* b = sB + st.idx * b_stage_bytes;
+                    for (int a = 0; a < kp / 64; ++a)
+                        tma_load_2d(b + a * nt * 128, &tm_b, &full[st.idx], ks * kp + a * 64, tile.y, pol_b);
+                    issued |= 1u << st.idx;
+                    last_parity = (last_parity & ~(1u << st.idx)) | (st.phase << st.idx);
+                    st.next(nstage);
+                }
+            }
+            // No copy may still be in flight when the CTA exits: wait for the
+            // last issue of every slot (already complete on the normal path).
+            for (int i = 0; i < nstage; ++i) {
+                if (!(issued & (1u << i))) continue;
+                const uint32_t a = smem_u32(&full[i]);
+                const uint32_t ph = (last_parity >> i) & 1u;
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(a, ph)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        atomicExch(status, kStatusTimeout);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
+            const uint32_t acc0 = tmem;                     // row block 0 accumulator
+            const uint32_t acc1 = tmem + static_cast<uint32_t>(nt);
+            const uint32_t abase = tmem + static_cast<uint32_t>(2 * nt);
+            Ring st, ab;
+            uint32_t accphase = 0;
+            bool ok = true;
+            bool issued = false;
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                if (!mbar_wait_bounded(accempty, accphase ^ 1u, abort_flag, status)) break;
+                tc_fence_after();
+                uint32_t accumulate = 0;
+                for (int ks = 0; ks < ksteps && ok; ++ks) {
+                    if (!mbar_wait_bounded(&full[st.idx], st.phase, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bstage = smem_u32(sB + st.idx * b_stage_bytes);
+                    for (int c = 0; c < chunks; ++c) {
+                        if (!mbar_wait_bounded(&afull[ab.idx], ab.phase, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t a0 = abase + ab.idx * 64;
+                        const uint32_t batom = bstage + static_cast<uint32_t>(c * nt * 128);
+#pragma unroll
+                        for (int k16 = 0; k16 < 4; ++k16) {
+                            const uint64_t bd = smem_desc_sw128(batom + k16 * 32);
+                            tc_mma_ts(acc0, a0 + k16 * 8, bd, idesc, accumulate);
+                            tc_mma_ts(acc1, a0 + 32 + k16 * 8, bd, idesc, accumulate);
+                            accumulate = 1;
+                        }
+                        issued = true;
+                        tc_commit(&aempty[ab.idx]);
+                        ab.next(kNumABuf);
+                    }
+                    if (!ok) break;
+                    tc_commit(&empty[st.idx]);
+                    st.next(nstage);
+                }
+                if (!ok) break;
+                tc_commit(accfull);
+                accphase ^= 1u;
+            }
+            if (!ok && issued) {
+                // make sure no MMA is still running before TMEM is released
+                tc_commit(drain);
+                const uint32_t a = smem_u32(drain);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(a, 0)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+                }
+            }
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ scale loader
+        Ring sb;
+        const int ng = p.ngroups;
+        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+            if (!mbar_wait_bounded(&sempty[sb.idx], sb.phase ^ 1u, abort_flag, status)) break;
+            const int4 tile = p.tiles[u / p.mt_count];
+            int r0, r1;
+            unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
+            uint16_t* dst = sS + sb.idx * (ng * 2 * kRowsPerTile);
+            for (int r = lane; r < 2 * kRowsPerTile; r += 32) {
+                const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
+                const uint16_t* src = p.scales + static_cast<int64_t>(grow) * ng;
+                for (int g = 0; g < ng; ++g) dst[g * 2 * kRowsPerTile + r] = __ldg(src + g);
+            }
+            mbar_arrive(&sfull[sb.idx]);
+            sb.next(2);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ dequant + epilogue
+        const int blk = (warp - 4) >> 2;        // row block 0 or 1
+        const int quarter = warp & 3;           // TMEM lanes 32*quarter ..
+        const int row = quarter * 32 + lane;    // row within the block
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t xr = static_cast<uint32_t>((row * pitch) >> 7) & static_cast<uint32_t>(pitch / 16 - 1);
+        const uint32_t abase = tmem + static_cast<uint32_t>(2 * nt) + lane_base + static_cast<uint32_t>(blk * 32);
+        const float L = p.limit;
+        Ring st, ab, sb;
+        uint32_t accphase = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            const int4 tile = p.tiles[u / p.mt_count];
+            const int mt = u % p.mt_count;
+            if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
+            const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + blk * kRowsPerTile + row;
+            for (int ks = 0; ks < ksteps && ok; ++ks) {
+                if (!mbar_wait_bounded(&full[st.idx], st.phase, abort_flag, status)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* wrow = sW + st.idx * 2 * w_tile_bytes + blk * w_tile_bytes + row * pitch;
+                for (int c = 0; c < chunks; ++c) {
+                    const int k0 = ks * kp + c * kKA;
+                    const float s = __half2float(__ushort_as_half(srow[(k0 / p.group) * 2 * kRowsPerTile]));
+                    uint32_t v[32];
+                    dequant_chunk<BITS>(wrow, xr, c, s, v);
+                    if (!mbar_wait_bounded(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tc_st_32x32b_x32(abase + ab.idx * 64, v);
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&afull[ab.idx]);
+                    ab.next(kNumABuf);
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[st.idx]);
+                st.next(nstage);
+            }
+            if (!ok) break;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sempty[sb.idx]);
+            sb.next(2);
+
+            // epilogue
+            if (!mbar_wait_bounded(accfull, accphase, abort_flag, status)) break;
+            tc_fence_after();
+            const int rows = tile.z;
+            const int row0 = tile.y;
+            if constexpr (W13) {
+                // both blocks read gate (acc0) and up (acc1) of their lane; block 0
+                // takes the first half of the tokens, block 1 the second half
+                const int half = nt / 2;
+                const int n = mt * kRowsPerTile + row;
+                for (int j0 = blk * half; j0 < (blk + 1) * half; j0 += 8) {
+                    uint32_t g[8], uu[8];
+                    tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(j0), g);
+                    tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(nt + j0), uu);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (j0 + i < rows) {
+                            const float hv = swiglu(__uint_as_float(g[i]), __uint_as_float(uu[i]), L);
+                            p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + n] = __float2bfloat16_rn(hv);
+                        }
+                    }
+                }
+            } else {
+                const int m = mt * 2 * kRowsPerTile + blk * kRowsPerTile + row;
+                const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(blk * nt);
+                for (int j0 = 0; j0 < nt; j0 += 8) {
+                    uint32_t d[8];
+                    tc_ld_32x32b_x8(acc + static_cast<uint32_t>(j0), d);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (j0 + i < rows)
+                            p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + m] =
+                                __float2bfloat16_rn(__uint_as_float(d[i]));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(accempty);
+            accphase ^= 1u;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
+    GemmSmem L{};
+    const int pitch = kp * bits / 8;
+    const int b_stage = (kp / 64) * nt * 128;
+    const int w_stage = 2 * kRowsPerTile * pitch;
+    const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
+    const int bar_bytes = 8 * (2 * 16 + 2 * kNumABuf + 2 + 4 + 1) + 16;
+    const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
+    int ns = (max_smem - fixed) / (b_stage + w_stage);
+    if (ns > 8) ns = 8;
+    L.nstage = ns;
+    if (ns < 2) return L;
+    L.off_b = 0;
+    L.off_w = ns * b_stage;
+    L.off_s = L.off_w + ns * w_stage;
+    L.off_bar = (L.off_s + s_bytes + 7) & ~7;
+    L.total = L.off_bar + 8 * (2 * ns + 2 * kNumABuf + 2 + 4 + 1) + 16 + 1024;
+    return L;
+}
+
+template <int BITS, bool W13>
+static cudaError_t launch_impl(const CUtensorMap& tm_w, const CUtensorMap& tm_b, const GemmParams& p, int grid,
+                               int smem_bytes, cudaStream_t stream) {
+    auto kern = grouped_gemm_kernel<BITS, W13>;
+    static int attr_bytes = 0;   // largest dynamic smem size already allowed for this kernel
+    if (smem_bytes > attr_bytes) {
+        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (err != cudaSuccess) return err;
+        attr_bytes = smem_bytes;
+    }
+    kern<<<grid, kThreads, smem_bytes, stream>>>(tm_w, tm_b, p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, const CUtensorMap& tm_b,
+                                const GemmParams& p, int grid, int smem_bytes, cudaStream_t stream) {
+    if (bits == 2)
+        return w13 ? launch_impl<2, true>(tm_w, tm_b, p, grid, smem_bytes, stream)
+                   : launch_impl<2, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
+    return w13 ? launch_impl<4, true>(tm_w, tm_b, p, grid, smem_bytes, stream)
+               : launch_impl<4, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
+}
+
+}  // namespace wna16

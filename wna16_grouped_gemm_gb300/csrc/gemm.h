@@ -1,0 +1,53 @@
+// Internal interface of the grouped WNA16 GEMM kernel (not part of the C ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace wna16 {
+
+struct GemmParams {
+    const int4* tiles;          // token tiles: {expert, first permuted row, rows, 0}
+    const int* n_tiles;         // number of valid tiles (device)
+    const uint16_t* scales;     // fp16 [E * rows_per_expert, ngroups]
+    __nv_bfloat16* out;         // h [R, N] (w13) or y [R, K] (w2), permuted rows
+    int out_ld;                 // row length of `out`
+    int rows_per_expert;        // 2N (w13) or K (w2)
+    int half_rows;              // N (w13: first up row)
+    int kred;                   // reduction length: K (w13) or N (w2)
+    int ngroups;                // kred / group
+    int group;                  // scale group along the reduction dim
+    int mt_count;               // 256-row units per expert: N/128 (w13) or K/256 (w2)
+    int kp;                     // K elements per pipeline stage
+    int nt;                     // token tile (MMA N): 16, 32, 64 or 128
+    int nstage;                 // smem pipeline depth
+    int off_b, off_w, off_s, off_bar;   // smem layout (bytes from the 1024-aligned base)
+    float limit;                // SwiGLU limit (w13 only)
+    int* status;                // device status word
+};
+
+struct GemmSmem {
+    int nstage = 0;
+    int off_b = 0, off_w = 0, off_s = 0, off_bar = 0;
+    int total = 0;
+};
+
+// Shared-memory plan for one launch; nstage < 2 means it does not fit.
+GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem);
+
+cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, const CUtensorMap& tm_b,
+                                const GemmParams& p, int grid, int smem_bytes, cudaStream_t stream);
+
+// Routing / gather / combine / pack kernels (kernels.cu).
+cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
+                         int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream);
+cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
+                          int K, __nv_bfloat16* xp, cudaStream_t stream);
+cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
+                           __nv_bfloat16* out, cudaStream_t stream);
+cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
+                        cudaStream_t stream);
+
+}  // namespace wna16

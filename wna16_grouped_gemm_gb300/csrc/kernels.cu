@@ -1,0 +1,245 @@
+// Routing/permute, gather, weighted combine and pack kernels of the WNA16
+// routed-expert MoE forward ("Incubate DeepSeek V4 WNA16 runtime on SM86",
+// section "What this branch adds", item 3: the indexed MoE; page
+// "hampsonw/DeepSeek-V4-Flash-0731-WNA16", section "How it was created",
+// step 4: packing signed codes into INT32 words).
+#include <cuda_bf16.h>
+
+#include "gemm.h"
+#include "ptx.cuh"
+
+namespace wna16 {
+
+namespace {
+
+constexpr int kRouteThreads = 1024;
+constexpr int kRouteWarps = kRouteThreads / 32;
+
+// Block-wide exclusive scan of two values with warp-level inclusive scans
+// (shuffles) and one pass over the 32 warp totals.
+__device__ __forceinline__ void block_exclusive_scan2(int a, int b, int& ea, int& eb, int& total_a, int& total_b,
+                                                      int* scratch /* 64 ints */) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int ia = a, ib = b;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int ta = __shfl_up_sync(0xffffffffu, ia, d);
+        const int tb = __shfl_up_sync(0xffffffffu, ib, d);
+        if (lane >= d) {
+            ia += ta;
+            ib += tb;
+        }
+    }
+    if (lane == 31) {
+        scratch[warp] = ia;
+        scratch[32 + warp] = ib;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int va = scratch[lane], vb = scratch[32 + lane];
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int ta = __shfl_up_sync(0xffffffffu, va, d);
+            const int tb = __shfl_up_sync(0xffffffffu, vb, d);
+            if (lane >= d) {
+                va += ta;
+                vb += tb;
+            }
+        }
+        scratch[lane] = va;           // inclusive warp prefix
+        scratch[32 + lane] = vb;
+    }
+    __syncthreads();
+    const int pa = warp ? scratch[warp - 1] : 0;
+    const int pb = warp ? scratch[32 + warp - 1] : 0;
+    ea = pa + ia - a;
+    eb = pb + ib - b;
+    total_a = scratch[31];
+    total_b = scratch[63];
+}
+
+// One CTA.  Slot f = t*topk + j.  Each warp owns a contiguous run of slots;
+// pass 1 counts its slots per expert (warp-match groups), a scan over warps and
+// over experts turns the counts into start positions, pass 2 places each slot
+// (stable: ascending slot within an expert) and records the inverse map.
+// Also emits the token-tile list {expert, first row, rows} in expert order.
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const int32_t* __restrict__ ids, int R, int E, int nt, int* __restrict__ counts,
+                 int* __restrict__ offsets, int* __restrict__ perm, int* __restrict__ inv, int4* __restrict__ tiles,
+                 int* __restrict__ n_tiles, int* __restrict__ status) {
+    extern __shared__ int sm[];
+    int* cnt = sm;                          // [kRouteWarps][E]
+    int* scratch = sm + kRouteWarps * E;    // 64 ints
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) *status = kStatusOk;
+
+    const int per_warp = (((R + kRouteWarps - 1) / kRouteWarps) + 31) & ~31;
+    const int f0 = warp * per_warp;
+    const int f1 = min(R, f0 + per_warp);
+    int* my = cnt + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+
+    bool bad = false;
+    for (int base = f0; base < f1; base += 32) {
+        const int f = base + lane;
+        int e = -1;
+        if (f < f1) {
+            e = ids[f];
+            if (e < 0 || e >= E) {
+                bad = true;
+                e = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    if (bad) atomicExch(status, kStatusBadRouting);
+
+    int c = 0;
+    if (tid < E) {
+        for (int w = 0; w < kRouteWarps; ++w) {
+            const int v = cnt[w * E + tid];
+            cnt[w * E + tid] = c;
+            c += v;
+        }
+    }
+    const int ntl = tid < E ? (c + nt - 1) / nt : 0;
+    int off, toff, total, ttotal;
+    block_exclusive_scan2(c, ntl, off, toff, total, ttotal, scratch);
+    if (tid < E) {
+        counts[tid] = c;
+        offsets[tid] = off;
+        for (int j = 0; j < ntl; ++j) tiles[toff + j] = make_int4(tid, off + j * nt, min(nt, c - j * nt), 0);
+        for (int w = 0; w < kRouteWarps; ++w) cnt[w * E + tid] += off;
+    }
+    if (tid == 0) {
+        offsets[E] = total;
+        *n_tiles = ttotal;
+    }
+    __syncthreads();
+
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = f0; base < f1; base += 32) {
+        const int f = base + lane;
+        int e = -1;
+        if (f < f1) {
+            e = ids[f];
+            if (e < 0 || e >= E) e = -1;
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int pos = e >= 0 ? my[e] + __popc(peers & lt) : -1;
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+        if (f < f1) {
+            if (e >= 0) perm[pos] = f;
+            inv[f] = pos;
+        }
+    }
+}
+
+// Xp[i, :] = x[perm[i] / topk, :] for the valid rows i < offsets[E].
+__global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
+                              const int* __restrict__ offsets_end, int topk, int vec_per_row,
+                              uint4* __restrict__ xp) {
+    const int i = blockIdx.x;
+    if (i >= *offsets_end) return;
+    const int64_t t = perm[i] / topk;
+    const uint4* src = x + t * vec_per_row;
+    uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
+    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
+}
+
+// out[t, m] = bf16( sum_j w[t, j] * y[inv[t*topk + j], m] ), fp32, j ascending;
+// a slot whose inverse index is -1 (bad expert id) adds nothing.
+__global__ void combine_kernel(const uint4* __restrict__ y, const float* __restrict__ w, const int* __restrict__ inv,
+                               int topk, int vec_per_row, uint4* __restrict__ out) {
+    const int t = blockIdx.y;
+    const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= vec_per_row) return;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < topk; ++j) {
+        const int r = inv[t * topk + j];
+        if (r < 0) continue;
+        const float wj = w[t * topk + j];
+        const uint4 q = __ldg(y + static_cast<int64_t>(r) * vec_per_row + v);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            acc[2 * i] = __fmaf_rn(wj, f.x, acc[2 * i]);
+            acc[2 * i + 1] = __fmaf_rn(wj, f.y, acc[2 * i + 1]);
+        }
+    }
+    uint4 o;
+    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    out[static_cast<int64_t>(t) * vec_per_row + v] = o;
+}
+
+// word i <- codes [i*p, (i+1)*p): field j = (code_j + 2^(b-1)) & (2^b - 1) at bits [b*j, b*j+b).
+__global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t n_words, int bits, int32_t* __restrict__ packed) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n_words) return;
+    const int p = 32 / bits;
+    const int off = 1 << (bits - 1);
+    const uint32_t mask = (1u << bits) - 1u;
+    const int8_t* c = codes + i * p;
+    uint32_t w = 0;
+    for (int j = 0; j < p; ++j) w |= (static_cast<uint32_t>(c[j] + off) & mask) << (bits * j);
+    packed[i] = static_cast<int32_t>(w);
+}
+
+}  // namespace
+
+cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm, int* inv,
+                         int4* tiles, int* n_tiles, int* status, cudaStream_t stream) {
+    const int smem = (kRouteWarps * E + 64) * static_cast<int>(sizeof(int));
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (kRouteWarps * 1024 + 64) * static_cast<int>(sizeof(int)));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, nt, counts, offsets, perm, inv, tiles, n_tiles,
+                                                    status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
+                          __nv_bfloat16* xp, cudaStream_t stream) {
+    if (R == 0) return cudaSuccess;
+    const int vpr = K / 8;
+    const int threads = vpr >= 256 ? 256 : 32;
+    gather_kernel<<<R, threads, 0, stream>>>(reinterpret_cast<const uint4*>(x), perm, offsets_end, topk, vpr,
+                                             reinterpret_cast<uint4*>(xp));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
+                           __nv_bfloat16* out, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int vpr = K / 8;
+    const int threads = 128;
+    dim3 grid((vpr + threads - 1) / threads, T);
+    combine_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(y), weights, inv, topk, vpr,
+                                                 reinterpret_cast<uint4*>(out));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
+                        cudaStream_t stream) {
+    const int64_t n_words = rows * (K * bits / 32);
+    if (n_words == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = (n_words + threads - 1) / threads;
+    pack_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(codes, n_words, bits, packed);
+    return cudaGetLastError();
+}
+
+}  // namespace wna16
