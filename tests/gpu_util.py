@@ -1,7 +1,10 @@
 """Helpers for the GPU parity tests: host inputs -> device tensors, oracle
 runs on the host, and the comparison metrics with the tolerances of the
-path (BF16 outputs: max-abs <= 2e-2 and relative L2 <= 1e-3; routing
-indices and packed words: bit-exact)."""
+path (routing indices and packed words: bit-exact; BF16 tensors: relative
+L2 <= 1e-3, and max-abs <= 2e-2 where the BF16 spacing of the reference
+value is finer than that -- an element whose reference has a BF16 ulp above
+2e-2 (|ref| >= 4) may differ by that one ulp, the smallest difference BF16
+can express there)."""
 from __future__ import annotations
 
 import numpy as np
@@ -47,7 +50,11 @@ def compare_bf16(got_bits, ref_bits, what: str = "") -> dict:
     ri = np.asarray(ref_bits, np.uint16).astype(np.int32)
     # ulp distance of bf16 patterns (same sign assumed for nearby values)
     ulp = np.abs(gi - ri)
+    # one BF16 ulp of each reference value (spacing above |ref|)
+    ulp_ref = np.ldexp(1.0, np.frexp(np.maximum(np.abs(r), 2.0 ** -126))[1] - 8)
+    allowed = np.maximum(MAX_ABS, ulp_ref)
     stats = dict(what=what, n=int(g.size), max_abs=float(d.max()) if d.size else 0.0, rel_l2=rel,
+                 max_abs_excess=float((d - allowed).max()) if d.size else 0.0,
                  exact=float((ulp == 0).mean()) if ulp.size else 1.0,
                  le1ulp=float((ulp <= 1).mean()) if ulp.size else 1.0,
                  nonfinite=int((~np.isfinite(g)).sum()))
@@ -58,5 +65,9 @@ def assert_close(got_bits, ref_bits, what: str = "", max_abs=MAX_ABS, rel_l2=REL
     s = compare_bf16(got_bits, ref_bits, what)
     print(s)
     assert s["nonfinite"] == 0, s
-    assert s["max_abs"] <= max_abs and s["rel_l2"] <= rel_l2, s
+    assert s["rel_l2"] <= rel_l2, s
+    if max_abs == MAX_ABS:
+        assert s["max_abs_excess"] <= 0.0, s
+    else:
+        assert s["max_abs"] <= max_abs, s
     return s

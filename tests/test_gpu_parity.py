@@ -83,6 +83,8 @@ def test_route_bit_exact(moe, oracle, T, topk, E, zipf):
 
 STAGE_CASES = [
     ("tiny_w2", None),
+    ("decode_w2", None),
+    ("decode_w4", None),
     ("small_w4", _small(bits=4, g13=128, g2=128)),
     ("small_w2_g64", _small(bits=2, g13=64, g2=64, T=53)),
     ("small_w4_g64_w2", _small(bits=4, g13=128, g2=64, T=300, E=3)),   # prefill-sized tiles

@@ -66,19 +66,51 @@ int choose_nt(int64_t R, int64_t E) {
     return 128;
 }
 
+// Split-K plan of one grouped GEMM: the smallest power of two (<= 8) that gives
+// at least kTargetItems work items over the largest possible unit count, with
+// every split a whole number of pipeline stages and scale groups.  Decided from
+// the sizes alone, so the workspace size needs no device query.
+constexpr int64_t kTargetItems = 1280;
+
+int stage_k(int nt, int bits, int64_t kred) {
+    if (nt > 32) return 64;
+    int kp = 1024 / bits;                       // 128 packed bytes per row per stage
+    while (kred % kp) kp /= 2;
+    return kp;
+}
+
+int choose_split(int64_t max_units, int64_t kred, int kp, int group) {
+    int S = 1;
+    while (S < 8 && max_units * S < kTargetItems) {
+        const int64_t next = 2 * S;
+        if ((kred / kp) % next || (kred / next) % group) break;
+        S = static_cast<int>(next);
+    }
+    return S;
+}
+
 struct Layout {
     int64_t R = 0;
     int nt = 16;
     int64_t max_tiles = 0;
+    int64_t units13 = 0, units2 = 0;      // largest possible unit counts of the two GEMMs
     size_t status = 0, n_tiles = 0, counts = 0, offsets = 0, perm = 0, inv = 0, tiles = 0, xp = 0, h = 0, y = 0;
+    size_t counters13 = 0, counters2 = 0, partial = 0;
     size_t total = 0;
 };
 
-Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk) {
+Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bits) {
     Layout L;
     L.R = T * topk;
     L.nt = choose_nt(L.R, E);
     L.max_tiles = (L.R < E ? L.R : E) + L.R / L.nt + 1;
+    L.units13 = L.max_tiles * (N / 128);
+    L.units2 = L.max_tiles * (K / 256);
+    // partial sums for the largest split any group size could give (64 is the
+    // smallest supported group): items x 256 rows x nt fp32
+    const int64_t items13 = L.units13 * choose_split(L.units13, K, stage_k(L.nt, bits, K), 64);
+    const int64_t items2 = L.units2 * choose_split(L.units2, N, stage_k(L.nt, bits, N), 64);
+    const int64_t items = items13 > items2 ? items13 : items2;
     size_t o = 0;
     L.status = o;   o = align_up(o + sizeof(int));
     L.n_tiles = o;  o = align_up(o + sizeof(int));
@@ -90,6 +122,9 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk) {
     L.xp = o;       o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
     L.h = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * N);
     L.y = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
+    L.counters13 = o; o = align_up(o + sizeof(int) * L.units13);
+    L.counters2 = o;  o = align_up(o + sizeof(int) * L.units2);
+    L.partial = o;  o = align_up(o + (items > L.units13 && items > L.units2 ? sizeof(float) * items * 256 * L.nt : 0));
     L.total = o;
     return L;
 }
@@ -220,7 +255,8 @@ int check_workspace(const void* ws, size_t bytes, const Layout& L) {
 int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStream_t s) {
     cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), L.nt, at<int>(ws, L.counts),
                                  at<int>(ws, L.offsets), at<int>(ws, L.perm), at<int>(ws, L.inv),
-                                 at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status), s);
+                                 at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status),
+                                 at<int>(ws, L.counters13), static_cast<int>((L.partial - L.counters13) / sizeof(int)), s);
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "route kernel launch");
 }
 
@@ -243,14 +279,11 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     const int64_t kred = w13 ? K : N;
     const int64_t rows_per_expert = w13 ? 2 * N : K;
     const int nt = L.nt;
-    int kp;
-    if (nt <= 32) {
-        kp = 1024 / bits;                       // 128 packed bytes per row per stage
-        while (kred % kp) kp /= 2;
-    } else {
-        kp = 64;
-    }
+    const int kp = stage_k(nt, bits, kred);
     const int pitch = kp * bits / 8;
+    const int64_t max_units = w13 ? L.units13 : L.units2;
+    const int ksplit = choose_split(max_units, kred, kp, group);
+    const bool row_boxes = nt <= 32;
     const int ngroups = static_cast<int>(kred / group);
     GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups, dev.max_smem);
     if (sm.nstage < 2) return fail(WNA16_ERR_UNSUPPORTED, "shared-memory plan does not fit");
@@ -261,7 +294,8 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
                            static_cast<uint32_t>(pitch / 4), swizzle_for_pitch(pitch)))
         return rc;
     if (int rc = encode_2d(&P.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b_src, static_cast<uint64_t>(L.R),
-                           static_cast<uint64_t>(kred), static_cast<uint32_t>(nt), 64, CU_TENSOR_MAP_SWIZZLE_128B))
+                           static_cast<uint64_t>(kred), row_boxes ? 1u : static_cast<uint32_t>(nt), 64,
+                           CU_TENSOR_MAP_SWIZZLE_128B))
         return rc;
 
     GemmParams& gp = P.gp;
@@ -285,9 +319,13 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.off_bar = sm.off_bar;
     gp.limit = limit;
     gp.status = at<int>(ws, L.status);
+    gp.ksplit = ksplit;
+    gp.partial = ksplit > 1 ? at<float>(ws, L.partial) : nullptr;
+    gp.counters = at<int>(ws, w13 ? L.counters13 : L.counters2);
+    gp.row_boxes = row_boxes ? 1 : 0;
 
-    const int64_t max_units = L.max_tiles * gp.mt_count;
-    P.grid = static_cast<int>(max_units < dev.sms ? max_units : dev.sms);
+    const int64_t max_items = max_units * ksplit;
+    P.grid = static_cast<int>(max_items < dev.sms ? max_items : dev.sms);
     P.smem = sm.total;
     P.w13 = w13;
     P.bits = bits;
@@ -309,7 +347,7 @@ const char* wna16_moe_last_error(void) { return g_err; }
 
 size_t wna16_moe_workspace_size(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bits) {
     if (check_dims(T, K, N, E, topk, bits) != WNA16_OK) return 0;
-    return make_layout(T, K, N, E, topk).total;
+    return make_layout(T, K, N, E, topk, bits).total;
 }
 
 int wna16_moe_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed, void* stream) {
@@ -358,7 +396,7 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
         const uintptr_t bytes = static_cast<uintptr_t>(T * K * 2);
         if (xb < ob + bytes && ob < xb + bytes) return fail(WNA16_ERR_INVALID_ARG, "out overlaps x");
     }
-    const Layout L = make_layout(T, K, N, E, topk);
+    const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmPlan p13, p2;
@@ -439,7 +477,7 @@ int wna16_moe_route(const int32_t* topk_ids, int64_t T, int topk, int64_t E, int
                     size_t workspace_bytes, void* stream) {
     g_err[0] = 0;
     if (int rc = check_dims(T, K, N, E, topk, bits)) return rc;
-    const Layout L = make_layout(T, K, N, E, topk);
+    const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     if (T > 0)
         if (int rc = check_ptr(topk_ids, 4, "topk_ids")) return rc;
@@ -473,7 +511,7 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
     if (int rc = check_ptr(topk_ids, 4, "topk_ids")) return rc;
     if (int rc = check_ptr(w13_packed, 16, "w13_packed")) return rc;
     if (int rc = check_ptr(w13_scales, 2, "w13_scales")) return rc;
-    const Layout L = make_layout(T, K, N, E, topk);
+    const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmPlan p13;
@@ -499,7 +537,7 @@ int wna16_moe_w2(const void* h, const int32_t* w2_packed, const uint16_t* w2_sca
     if (int rc = check_ptr(y_out, 16, "y_out")) return rc;
     if (int rc = check_ptr(w2_packed, 16, "w2_packed")) return rc;
     if (int rc = check_ptr(w2_scales, 2, "w2_scales")) return rc;
-    const Layout L = make_layout(T, K, N, E, topk);
+    const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     GemmPlan p2;
     if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, h, y_out, K, N, E, group_size_w2, INFINITY, L,
@@ -516,7 +554,7 @@ int wna16_moe_combine(const void* y, const float* topk_weights, int64_t T, int64
     if (int rc = check_ptr(y, 16, "y")) return rc;
     if (int rc = check_ptr(out, 16, "out")) return rc;
     if (int rc = check_ptr(topk_weights, 4, "topk_weights")) return rc;
-    const Layout L = make_layout(T, K, N, E, topk);
+    const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaError_t e = launch_combine(static_cast<const __nv_bfloat16*>(y), topk_weights, at<int>(workspace, L.inv),
                                    static_cast<int>(T), topk, static_cast<int>(K), static_cast<__nv_bfloat16*>(out),

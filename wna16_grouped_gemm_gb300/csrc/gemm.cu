@@ -195,8 +195,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* sfull = accempty + 1;
     uint64_t* sempty = sfull + 2;
     uint64_t* drain = sempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* pdone = drain + 1;      // split K: all epilogue warps parked their partial sums
+    uint64_t* pflag = pdone + 1;      // split K: arrival counted, last_flag is valid
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pflag + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nstage; ++i) {
@@ -214,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sempty[i], 8);
         }
         mbar_init(drain, 1);
+        mbar_init(pdone, 8);
+        mbar_init(pflag, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_w);
@@ -229,6 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
 
     const int n_units = (*p.n_tiles) * p.mt_count;
+    const int ksplit = p.ksplit;
+    const int n_items = n_units * ksplit;         // item = (unit, K split)
+    const int kps = ksteps / ksplit;              // stages per item
     int* status = p.status;
 
     if (warp == 0) {
@@ -240,23 +248,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             Ring st;
             uint32_t issued = 0, last_parity = 0;   // per slot: issued at least once / parity of last issue
             bool ok = true;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
+                const int u = v / ksplit;
+                const int split = v - u * ksplit;
                 const int4 tile = p.tiles[u / p.mt_count];
                 int r0, r1;
                 unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
-                for (int ks = 0; ks < ksteps; ++ks) {
+                // decode tiles: only the tile's real rows are fetched, one row per box
+                const uint32_t tx_item =
+                    p.row_boxes ? static_cast<uint32_t>(2 * w_tile_bytes + (kp / 64) * tile.z * 128) : tx;
+                for (int ks = split * kps; ks < (split + 1) * kps; ++ks) {
                     if (!mbar_wait_bounded(&empty[st.idx], st.phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[st.idx], tx);
+                    mbar_arrive_expect_tx(&full[st.idx], tx_item);
                     uint8_t* w = sW + st.idx * 2 * w_tile_bytes;
                     const int wc = ks * (kp / kCodes);
                     tma_load_2d(w, &tm_w, &full[st.idx], wc, r0, pol_w);
                     tma_load_2d(w + w_tile_bytes, &tm_w, &full[st.idx], wc, r1, pol_w);
                     uint8_t* b = sB + st.idx * b_stage_bytes;
-                    for (int a = 0; a < kp / 64; ++a)
-                        tma_load_2d(b + a * nt * 128, &tm_b, &full[st.idx], ks * kp + a * 64, tile.y, pol_b);
+                    if (p.row_boxes) {
+                        for (int a = 0; a < kp / 64; ++a)
+                            for (int r = 0; r < tile.z; ++r)
+                                tma_load_2d(b + a * nt * 128 + r * 128, &tm_b, &full[st.idx], ks * kp + a * 64,
+                                            tile.y + r, pol_b);
+                    } else {
+                        for (int a = 0; a < kp / 64; ++a)
+                            tma_load_2d(b + a * nt * 128, &tm_b, &full[st.idx], ks * kp + a * 64, tile.y, pol_b);
+                    }
                     issued |= 1u << st.idx;
                     last_parity = (last_parity & ~(1u << st.idx)) | (st.phase << st.idx);
                     st.next(nstage);
@@ -288,11 +308,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t accphase = 0;
             bool ok = true;
             bool issued = false;
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
                 if (!mbar_wait_bounded(accempty, accphase ^ 1u, abort_flag, status)) break;
                 tc_fence_after();
                 uint32_t accumulate = 0;
-                for (int ks = 0; ks < ksteps && ok; ++ks) {
+                for (int ks = 0; ks < kps && ok; ++ks) {
                     if (!mbar_wait_bounded(&full[st.idx], st.phase, abort_flag, status)) {
                         ok = false;
                         break;
@@ -339,16 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ scale loader
         Ring sb;
         const int ng = p.ngroups;
-        for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+        const int ng_item = ng / ksplit;           // groups of one K split
+        for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
             if (!mbar_wait_bounded(&sempty[sb.idx], sb.phase ^ 1u, abort_flag, status)) break;
+            const int u = v / ksplit;
+            const int g0 = (v - u * ksplit) * ng_item;
             const int4 tile = p.tiles[u / p.mt_count];
             int r0, r1;
             unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
             uint16_t* dst = sS + sb.idx * (ng * 2 * kRowsPerTile);
             for (int r = lane; r < 2 * kRowsPerTile; r += 32) {
                 const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
-                const uint16_t* src = p.scales + static_cast<int64_t>(grow) * ng;
-                for (int g = 0; g < ng; ++g) dst[g * 2 * kRowsPerTile + r] = __ldg(src + g);
+                const uint16_t* src = p.scales + static_cast<int64_t>(grow) * ng + g0;
+                for (int g = 0; g < ng_item; ++g) dst[g * 2 * kRowsPerTile + r] = __ldg(src + g);
             }
             mbar_arrive(&sfull[sb.idx]);
             sb.next(2);
@@ -363,14 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t abase = tmem + static_cast<uint32_t>(2 * nt) + lane_base + static_cast<uint32_t>(blk * 32);
         const float L = p.limit;
         Ring st, ab, sb;
-        uint32_t accphase = 0;
+        uint32_t accphase = 0, splitphase = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
+            const int u = v / ksplit;
+            const int split = v - u * ksplit;
+            const int kbeg = split * kps * kp;
             const int4 tile = p.tiles[u / p.mt_count];
             const int mt = u % p.mt_count;
             if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
             const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + blk * kRowsPerTile + row;
-            for (int ks = 0; ks < ksteps && ok; ++ks) {
+            for (int ks = split * kps; ks < (split + 1) * kps && ok; ++ks) {
                 if (!mbar_wait_bounded(&full[st.idx], st.phase, abort_flag, status)) {
                     ok = false;
                     break;
@@ -378,7 +404,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* wrow = sW + st.idx * 2 * w_tile_bytes + blk * w_tile_bytes + row * pitch;
                 for (int c = 0; c < chunks; ++c) {
                     const int k0 = ks * kp + c * kKA;
-                    const float s = __half2float(__ushort_as_half(srow[(k0 / p.group) * 2 * kRowsPerTile]));
+                    const float s =
+                        __half2float(__ushort_as_half(srow[((k0 - kbeg) / p.group) * 2 * kRowsPerTile]));
                     uint32_t v[32];
                     dequant_chunk<BITS>(wrow, xr, c, s, v);
                     if (!mbar_wait_bounded(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
@@ -408,6 +435,64 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int rows = tile.z;
             const int row0 = tile.y;
+            if (ksplit > 1) {
+                // Split K: park this split's fp32 sums (real token columns only);
+                // the last split of the unit to arrive adds all splits in split
+                // order (deterministic) and runs the epilogue.
+                float* mine = p.partial + static_cast<int64_t>(v) * (2 * kRowsPerTile * nt) +
+                              (blk * kRowsPerTile + row) * nt;
+                for (int j0 = 0; j0 < rows; j0 += 8) {
+                    uint32_t d[8];
+                    tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(blk * nt + j0), d);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (j0 + i < rows) __stcg(mine + j0 + i, __uint_as_float(d[i]));
+                }
+                tc_fence_before();
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(accempty);
+                    mbar_arrive(pdone);
+                }
+                accphase ^= 1u;
+                if (threadIdx.x == 128) {
+                    if (mbar_wait_bounded(pdone, splitphase, abort_flag, status)) {
+                        const int old = atomicAdd(&p.counters[u], 1);
+                        *last_flag = (old == ksplit - 1);
+                        if (old == ksplit - 1) p.counters[u] = 0;
+                    } else {
+                        *last_flag = 0;
+                    }
+                    mbar_arrive(pflag);
+                }
+                if (!mbar_wait_bounded(pflag, splitphase, abort_flag, status)) break;
+                splitphase ^= 1u;
+                if (!*last_flag) continue;
+                __threadfence();
+                const float* base = p.partial + static_cast<int64_t>(u) * ksplit * (2 * kRowsPerTile * nt) + row * nt;
+                const int stride = 2 * kRowsPerTile * nt;
+                if constexpr (W13) {
+                    const int n = mt * kRowsPerTile + row;
+                    for (int j = blk; j < rows; j += 2) {
+                        float g = 0.f, uu = 0.f;
+                        for (int q = 0; q < ksplit; ++q) {
+                            g += __ldcg(base + q * stride + j);
+                            uu += __ldcg(base + q * stride + kRowsPerTile * nt + j);
+                        }
+                        p.out[static_cast<int64_t>(row0 + j) * p.out_ld + n] = __float2bfloat16_rn(swiglu(g, uu, L));
+                    }
+                } else {
+                    const int m = mt * 2 * kRowsPerTile + blk * kRowsPerTile + row;
+                    for (int j = 0; j < rows; ++j) {
+                        float acc = 0.f;
+                        for (int q = 0; q < ksplit; ++q) acc += __ldcg(base + q * stride + blk * kRowsPerTile * nt + j);
+                        p.out[static_cast<int64_t>(row0 + j) * p.out_ld + m] = __float2bfloat16_rn(acc);
+                    }
+                }
+                continue;
+            }
             if constexpr (W13) {
                 // both blocks read gate (acc0) and up (acc1) of their lane; block 0
                 // takes the first half of the tokens, block 1 the second half
@@ -463,7 +548,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
     const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
-    const int bar_bytes = 8 * (2 * 16 + 2 * kNumABuf + 2 + 4 + 1) + 16;
+    const int bar_bytes = 8 * (2 * 16 + 2 * kNumABuf + 2 + 4 + 3) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);
     if (ns > 8) ns = 8;
@@ -473,7 +558,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     L.off_w = ns * b_stage;
     L.off_s = L.off_w + ns * w_stage;
     L.off_bar = (L.off_s + s_bytes + 7) & ~7;
-    L.total = L.off_bar + 8 * (2 * ns + 2 * kNumABuf + 2 + 4 + 1) + 16 + 1024;
+    L.total = L.off_bar + 8 * (2 * ns + 2 * kNumABuf + 2 + 4 + 3) + 16 + 1024;
     return L;
 }
 

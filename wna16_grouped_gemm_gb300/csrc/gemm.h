@@ -26,6 +26,10 @@ struct GemmParams {
     int off_b, off_w, off_s, off_bar;   // smem layout (bytes from the 1024-aligned base)
     float limit;                // SwiGLU limit (w13 only)
     int* status;                // device status word
+    int ksplit;                 // K splits per unit (1: no split)
+    float* partial;             // split-K partial sums [units * ksplit][2][128][nt] fp32
+    int* counters;              // split-K arrival counters [units], zero on entry
+    int row_boxes;              // 1: token tiles are loaded one real row at a time
 };
 
 struct GemmSmem {
@@ -42,7 +46,8 @@ cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, con
 
 // Routing / gather / combine / pack kernels (kernels.cu).
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
-                         int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream);
+                         int* inv, int4* tiles, int* n_tiles, int* status, int* zero, int n_zero,
+                         cudaStream_t stream);
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
                           int K, __nv_bfloat16* xp, cudaStream_t stream);
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,

@@ -66,12 +66,13 @@ __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int& ea, int
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_kernel(const int32_t* __restrict__ ids, int R, int E, int nt, int* __restrict__ counts,
                  int* __restrict__ offsets, int* __restrict__ perm, int* __restrict__ inv, int4* __restrict__ tiles,
-                 int* __restrict__ n_tiles, int* __restrict__ status) {
+                 int* __restrict__ n_tiles, int* __restrict__ status, int* __restrict__ zero, int n_zero) {
     extern __shared__ int sm[];
     int* cnt = sm;                          // [kRouteWarps][E]
     int* scratch = sm + kRouteWarps * E;    // 64 ints
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) *status = kStatusOk;
+    for (int i = tid; i < n_zero; i += kRouteThreads) zero[i] = 0;   // split-K arrival counters
 
     const int per_warp = (((R + kRouteWarps - 1) / kRouteWarps) + 31) & ~31;
     const int f0 = warp * per_warp;
@@ -197,7 +198,7 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t n_words, i
 }  // namespace
 
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm, int* inv,
-                         int4* tiles, int* n_tiles, int* status, cudaStream_t stream) {
+                         int4* tiles, int* n_tiles, int* status, int* zero, int n_zero, cudaStream_t stream) {
     const int smem = (kRouteWarps * E + 64) * static_cast<int>(sizeof(int));
     static bool attr_set = false;
     if (!attr_set) {
@@ -207,7 +208,7 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, 
         attr_set = true;
     }
     route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, nt, counts, offsets, perm, inv, tiles, n_tiles,
-                                                    status);
+                                                    status, zero, n_zero);
     return cudaGetLastError();
 }
 
