@@ -73,7 +73,7 @@ int choose_nt(int64_t R, int64_t E) {
 constexpr int64_t kTargetItems = 1280;
 
 int stage_k(int nt, int bits, int64_t kred) {
-    if (nt > 32) return 64;
+    if (nt > 32) return 128;
     int kp = 1024 / bits;                       // 128 packed bytes per row per stage
     while (kred % kp) kp /= 2;
     return kp;
@@ -106,11 +106,13 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.max_tiles = (L.R < E ? L.R : E) + L.R / L.nt + 1;
     L.units13 = L.max_tiles * (N / 128);
     L.units2 = L.max_tiles * (K / 256);
-    // partial sums for the largest split any group size could give (64 is the
-    // smallest supported group): items x 256 rows x nt fp32
-    const int64_t items13 = L.units13 * choose_split(L.units13, K, stage_k(L.nt, bits, K), 64);
-    const int64_t items2 = L.units2 * choose_split(L.units2, N, stage_k(L.nt, bits, N), 64);
-    const int64_t items = items13 > items2 ? items13 : items2;
+    // split-K partial sums for the largest split any group size could give (64
+    // is the smallest supported group): splits x row tiles x R token rows x 256
+    const int64_t s13 = choose_split(L.units13, K, stage_k(L.nt, bits, K), 64);
+    const int64_t s2 = choose_split(L.units2, N, stage_k(L.nt, bits, N), 64);
+    const int64_t p13 = s13 > 1 ? s13 * (N / 128) * L.R * 256 : 0;
+    const int64_t p2 = s2 > 1 ? s2 * (K / 256) * L.R * 256 : 0;
+    const int64_t partial_floats = p13 > p2 ? p13 : p2;
     size_t o = 0;
     L.status = o;   o = align_up(o + sizeof(int));
     L.n_tiles = o;  o = align_up(o + sizeof(int));
@@ -124,7 +126,7 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.y = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
     L.counters13 = o; o = align_up(o + sizeof(int) * L.units13);
     L.counters2 = o;  o = align_up(o + sizeof(int) * L.units2);
-    L.partial = o;  o = align_up(o + (items > L.units13 && items > L.units2 ? sizeof(float) * items * 256 * L.nt : 0));
+    L.partial = o;  o = align_up(o + sizeof(float) * partial_floats);
     L.total = o;
     return L;
 }
@@ -273,7 +275,8 @@ struct GemmPlan {
 };
 
 int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uint16_t* wscales, const void* b_src,
-              void* out, int64_t K, int64_t N, int64_t E, int group, float limit, const Layout& L, void* ws) {
+              void* out, int64_t K, int64_t N, int64_t E, int group, float limit, const Layout& L, void* ws,
+              bool h_interleaved = false) {
     DevInfo dev;
     if (int rc = device_info(dev)) return rc;
     const int64_t kred = w13 ? K : N;
@@ -313,6 +316,7 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.kp = kp;
     gp.nt = nt;
     gp.nstage = sm.nstage;
+    gp.nabuf = (512 - 2 * nt) / 128 < 3 ? (512 - 2 * nt) / 128 : 3;
     gp.off_b = sm.off_b;
     gp.off_w = sm.off_w;
     gp.off_s = sm.off_s;
@@ -321,8 +325,19 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.status = at<int>(ws, L.status);
     gp.ksplit = ksplit;
     gp.partial = ksplit > 1 ? at<float>(ws, L.partial) : nullptr;
+    gp.partial_rows = static_cast<int>(L.R);
     gp.counters = at<int>(ws, w13 ? L.counters13 : L.counters2);
     gp.row_boxes = row_boxes ? 1 : 0;
+    gp.h_interleaved = h_interleaved ? 1 : 0;
+    // widest async copy that divides the scale row stride, one split's row
+    // segment and the base alignment
+    gp.scale_copy_bytes = 0;
+    for (int c : {16, 8, 4}) {
+        if ((ngroups * 2) % c == 0 && ((ngroups / ksplit) * 2) % c == 0 && aligned(wscales, c)) {
+            gp.scale_copy_bytes = c;
+            break;
+        }
+    }
 
     const int64_t max_items = max_units * ksplit;
     P.grid = static_cast<int>(max_items < dev.sms ? max_items : dev.sms);
@@ -400,8 +415,11 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmPlan p13, p2;
+    // 2-bit weights are consumed in the interleaved 16-k order: x is gathered
+    // and h is written in that order (w2's input), y and out are not affected.
+    const bool il = bits == 2;
     if (int rc = plan_gemm(p13, true, bits, w13_packed, w13_scales, at<void>(workspace, L.xp),
-                           at<void>(workspace, L.h), K, N, E, group_size, swiglu_limit, L, workspace))
+                           at<void>(workspace, L.h), K, N, E, group_size, swiglu_limit, L, workspace, il))
         return rc;
     if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, at<void>(workspace, L.h), at<void>(workspace, L.y),
                            K, N, E, g2, swiglu_limit, L, workspace))
@@ -412,7 +430,7 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     mark(1, s);
     cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
-                                  static_cast<int>(K), at<__nv_bfloat16>(workspace, L.xp), s);
+                                  static_cast<int>(K), il ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     mark(2, s);
     if (int rc = launch_plan(p13, s)) return rc;
@@ -521,7 +539,7 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
     if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
     cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
-                                  static_cast<int>(K), at<__nv_bfloat16>(workspace, L.xp), s);
+                                  static_cast<int>(K), bits == 2 ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     return launch_plan(p13, s);
 }
@@ -539,11 +557,19 @@ int wna16_moe_w2(const void* h, const int32_t* w2_packed, const uint16_t* w2_sca
     if (int rc = check_ptr(w2_scales, 2, "w2_scales")) return rc;
     const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const void* b_src = h;
+    if (bits == 2) {   // 2-bit weights read h in the interleaved 16-k order
+        cudaError_t e = launch_interleave_rows(static_cast<const __nv_bfloat16*>(h), L.R, N, 0,
+                                               at<__nv_bfloat16>(workspace, L.h), s);
+        if (e != cudaSuccess) return cuda_fail(e, "interleave kernel launch");
+        b_src = at<void>(workspace, L.h);
+    }
     GemmPlan p2;
-    if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, h, y_out, K, N, E, group_size_w2, INFINITY, L,
+    if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, b_src, y_out, K, N, E, group_size_w2, INFINITY, L,
                            workspace))
         return rc;
-    return launch_plan(p2, static_cast<cudaStream_t>(stream));
+    return launch_plan(p2, s);
 }
 
 int wna16_moe_combine(const void* y, const float* topk_weights, int64_t T, int64_t K, int topk, int64_t E, int64_t N,

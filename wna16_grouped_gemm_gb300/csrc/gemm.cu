@@ -35,8 +35,8 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kRowsPerTile = 128;
-constexpr int kKA = 64;          // K elements per TMEM A buffer (per row block)
-constexpr int kNumABuf = 4;      // TMEM A ring
+constexpr int kKA = 128;         // K elements per TMEM A buffer (per row block): 64 columns
+constexpr int kMaxABuf = 3;      // TMEM A ring depth (fewer when the accumulators need the columns)
 constexpr int kTmemCols = 512;
 
 struct Ring {
@@ -51,13 +51,13 @@ struct Ring {
 
 // ------------------------------------------------------------------ dequant
 //
-// A b-bit field q placed at mantissa bit `pos` of a float whose exponent
-// field is (150 - pos) reads as 2^(23-pos) + q.  fma(that, s, -(2^(23-pos) +
-// 2^(b-1)) * s) then equals (q - 2^(b-1)) * s = code * s EXACTLY: the product
-// has at most 4 + 11 significant bits and the offset constant at most 13 + 11
-// <= 24 bits for the positions used (10..20 for 2-bit, 8..16 for 4-bit
-// fields), so the single rounding of the FMA has nothing to round.  One
-// cvt.rn.bf16x2 then gives the correctly rounded BF16 weights.
+// 4-bit fields: a field q placed at mantissa bit `pos` of a float whose
+// exponent field is (150 - pos) reads as 2^(23-pos) + q.  fma(that, s,
+// -(2^(23-pos) + 8) * s) then equals (q - 8) * s = code * s EXACTLY: the
+// product has at most 4 + 11 significant bits and the offset constant at most
+// 13 + 11 <= 24 bits for the positions used (8, 12, 16), so the single
+// rounding of the FMA has nothing to round.  One cvt.rn.bf16x2 then gives the
+// correctly rounded BF16 weights.
 template <int POS>
 __device__ __forceinline__ uint32_t magic_bits() {
     return static_cast<uint32_t>(150 - POS) << 23;
@@ -75,31 +75,55 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Constants -(2^(23-pos) + 2^(b-1)) * s for one scale.
-struct Neg2 {  // 2-bit: pos 10, 12, 14, 16, 18, 20
-    float c10, c12, c14, c16, c18, c20;
-    __device__ __forceinline__ explicit Neg2(float s)
-        : c10(-8194.0f * s), c12(-2050.0f * s), c14(-514.0f * s), c16(-130.0f * s), c18(-34.0f * s),
-          c20(-10.0f * s) {}
-};
+// Constants -(2^(23-pos) + 8) * s for one scale (4-bit fields).
 struct Neg4 {  // 4-bit: pos 8, 12, 16
     float c8, c12, c16;
     __device__ __forceinline__ explicit Neg4(float s) : c8(-32776.0f * s), c12(-2056.0f * s), c16(-136.0f * s) {}
 };
 
-// One 2-bit word (16 consecutive k) -> 8 bf16x2 (pairs k, k+1).
-__device__ __forceinline__ void dequant_word2(uint32_t w, float s, const Neg2& c, uint32_t* o) {
-    const uint32_t a = w << 12;   // fields 0..4 at bits 12..20
-    const uint32_t m = w;         // fields 5..10 at bits 10..20
-    const uint32_t r = w >> 12;   // fields 11..15 at bits 10..18
-    o[0] = pack_bf16x2(field_value<2, 12>(a, s, c.c12), field_value<2, 14>(a, s, c.c14));
-    o[1] = pack_bf16x2(field_value<2, 16>(a, s, c.c16), field_value<2, 18>(a, s, c.c18));
-    o[2] = pack_bf16x2(field_value<2, 20>(a, s, c.c20), field_value<2, 10>(m, s, c.c10));
-    o[3] = pack_bf16x2(field_value<2, 12>(m, s, c.c12), field_value<2, 14>(m, s, c.c14));
-    o[4] = pack_bf16x2(field_value<2, 16>(m, s, c.c16), field_value<2, 18>(m, s, c.c18));
-    o[5] = pack_bf16x2(field_value<2, 20>(m, s, c.c20), field_value<2, 10>(r, s, c.c10));
-    o[6] = pack_bf16x2(field_value<2, 12>(r, s, c.c12), field_value<2, 14>(r, s, c.c14));
-    o[7] = pack_bf16x2(field_value<2, 16>(r, s, c.c16), field_value<2, 18>(r, s, c.c18));
+// 2-bit fields: in BF16, 0x4300 is 128.0
+// with a unit last place, so OR-ing a field q into mantissa bits 2i..2i+1
+// reads 128 + 4^i q.  One bf16x2 add of -(128 + 2*4^i) gives 4^i * code exactly,
+// and one bf16x2 multiply by bf16(scale) / 4^i gives code * bf16(scale), which
+// for 2-bit codes (0 or +-2^j) IS bf16_rne(code * scale).  A register pairs
+// field c (low half) with field c+8 (high half) of a word, so within every
+// 16-k block the A operand's K order is (0, 8, 1, 9, ..., 7, 15); the token
+// operand is stored in that order too (gather kernel, w13 epilogue).
+__device__ __forceinline__ uint32_t bf2_add(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t bf2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+constexpr uint32_t kBf2Magic = 0x43004300u;    // (128.0, 128.0)
+constexpr uint32_t kBf2Neg130 = 0xC302C302u;   // -(128 + 2)
+constexpr uint32_t kBf2Neg136 = 0xC308C308u;   // -(128 + 8)
+constexpr uint32_t kBf2Neg160 = 0xC320C320u;   // -(128 + 32)
+
+struct Scale2 {  // bf16(s) / 4^i as bf16x2, i = 0, 1, 2
+    uint32_t s0, s1, s2;
+    __device__ __forceinline__ explicit Scale2(float s) {
+        const float sb = __bfloat162float(__float2bfloat16_rn(s));
+        s0 = pack_bf16x2(sb, sb);
+        s1 = pack_bf16x2(sb * 0.25f, sb * 0.25f);
+        s2 = pack_bf16x2(sb * 0.0625f, sb * 0.0625f);
+    }
+};
+
+__device__ __forceinline__ void dequant_word2_pairs(uint32_t w, const Scale2& c, uint32_t* o) {
+    const uint32_t w6 = w >> 6, w12 = w >> 12;
+    o[0] = bf2_mul(bf2_add((w & 0x00030003u) | kBf2Magic, kBf2Neg130), c.s0);    // fields 0, 8
+    o[1] = bf2_mul(bf2_add((w & 0x000C000Cu) | kBf2Magic, kBf2Neg136), c.s1);    // fields 1, 9
+    o[2] = bf2_mul(bf2_add((w & 0x00300030u) | kBf2Magic, kBf2Neg160), c.s2);    // fields 2, 10
+    o[3] = bf2_mul(bf2_add((w6 & 0x00030003u) | kBf2Magic, kBf2Neg130), c.s0);   // fields 3, 11
+    o[4] = bf2_mul(bf2_add((w6 & 0x000C000Cu) | kBf2Magic, kBf2Neg136), c.s1);   // fields 4, 12
+    o[5] = bf2_mul(bf2_add((w6 & 0x00300030u) | kBf2Magic, kBf2Neg160), c.s2);   // fields 5, 13
+    o[6] = bf2_mul(bf2_add((w12 & 0x00030003u) | kBf2Magic, kBf2Neg130), c.s0);  // fields 6, 14
+    o[7] = bf2_mul(bf2_add((w12 & 0x000C000Cu) | kBf2Magic, kBf2Neg136), c.s1);  // fields 7, 15
 }
 
 // One 4-bit word (8 consecutive k) -> 4 bf16x2.
@@ -121,11 +145,11 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t* row, uint32_t xr, i
                                               uint32_t (&o)[32]) {
     if constexpr (BITS == 2) {
         const uint4 v = *reinterpret_cast<const uint4*>(row + ((static_cast<uint32_t>(chunk) ^ xr) << 4));
-        const Neg2 c(s);
-        dequant_word2(v.x, s, c, o + 0);
-        dequant_word2(v.y, s, c, o + 8);
-        dequant_word2(v.z, s, c, o + 16);
-        dequant_word2(v.w, s, c, o + 24);
+        const Scale2 c(s);
+        dequant_word2_pairs(v.x, c, o + 0);
+        dequant_word2_pairs(v.y, c, o + 8);
+        dequant_word2_pairs(v.z, c, o + 16);
+        dequant_word2_pairs(v.w, c, o + 24);
     } else {
         const uint32_t j0 = static_cast<uint32_t>(2 * chunk);
         const uint4 v0 = *reinterpret_cast<const uint4*>(row + ((j0 ^ xr) << 4));
@@ -146,6 +170,13 @@ __device__ __forceinline__ float swiglu(float g, float u, float L) {
     g = fminf(g, L);
     u = fminf(fmaxf(u, -L), L);
     return g / (1.0f + expf(-g)) * u;
+}
+
+// Position of element k in the interleaved K order (0, 8, 1, 9, ..., 7, 15)
+// of a 16-k block.
+__device__ __forceinline__ int interleave16(int k) {
+    const int e = k & 15;
+    return (k & ~15) | (e < 8 ? 2 * e : 2 * (e - 8) + 1);
 }
 
 // Weight rows of the two 128-row blocks of unit (expert e, row tile mt).
@@ -181,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w_tile_bytes = kRowsPerTile * pitch;
     const int ksteps = p.kred / kp;
     const int chunks = kp / kKA;
+    const int nabuf = p.nabuf;
 
     uint8_t* sB = smem + p.off_b;
     uint8_t* sW = smem + p.off_w;
@@ -189,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* full = bars;
     uint64_t* empty = full + nstage;
     uint64_t* afull = empty + nstage;
-    uint64_t* aempty = afull + kNumABuf;
-    uint64_t* accfull = aempty + kNumABuf;
+    uint64_t* aempty = afull + kMaxABuf;
+    uint64_t* accfull = aempty + kMaxABuf;
     uint64_t* accempty = accfull + 1;
     uint64_t* sfull = accempty + 1;
     uint64_t* sempty = sfull + 2;
@@ -206,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 8 + 1);
         }
-        for (int i = 0; i < kNumABuf; ++i) {
+        for (int i = 0; i < kMaxABuf; ++i) {
             mbar_init(&afull[i], 8);
             mbar_init(&aempty[i], 1);
         }
@@ -232,6 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // everything above overlapped the previous kernel; its outputs (tiles,
+    // token rows) are read only below
+    pdl_wait();
+    pdl_trigger();
 
     const int n_units = (*p.n_tiles) * p.mt_count;
     const int ksplit = p.ksplit;
@@ -258,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tx_item =
                     p.row_boxes ? static_cast<uint32_t>(2 * w_tile_bytes + (kp / 64) * tile.z * 128) : tx;
                 for (int ks = split * kps; ks < (split + 1) * kps; ++ks) {
-                    if (!mbar_wait_bounded(&empty[st.idx], st.phase ^ 1u, abort_flag, status)) {
+                    if (!mbar_wait(&empty[st.idx], st.phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
@@ -313,29 +349,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 uint32_t accumulate = 0;
                 for (int ks = 0; ks < kps && ok; ++ks) {
-                    if (!mbar_wait_bounded(&full[st.idx], st.phase, abort_flag, status)) {
+                    if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t bstage = smem_u32(sB + st.idx * b_stage_bytes);
                     for (int c = 0; c < chunks; ++c) {
-                        if (!mbar_wait_bounded(&afull[ab.idx], ab.phase, abort_flag, status)) {
+                        if (!mbar_wait(&afull[ab.idx], ab.phase, abort_flag, status)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a0 = abase + ab.idx * 64;
-                        const uint32_t batom = bstage + static_cast<uint32_t>(c * nt * 128);
+                        const uint32_t a0 = abase + ab.idx * 128;
 #pragma unroll
-                        for (int k16 = 0; k16 < 4; ++k16) {
-                            const uint64_t bd = smem_desc_sw128(batom + k16 * 32);
+                        for (int k16 = 0; k16 < 8; ++k16) {
+                            // B: 64-k swizzle atom (2c + k16/4), 32 B per 16 k inside it
+                            const uint32_t batom =
+                                bstage + static_cast<uint32_t>((2 * c + (k16 >> 2)) * nt * 128 + (k16 & 3) * 32);
+                            const uint64_t bd = smem_desc_sw128(batom);
                             tc_mma_ts(acc0, a0 + k16 * 8, bd, idesc, accumulate);
-                            tc_mma_ts(acc1, a0 + 32 + k16 * 8, bd, idesc, accumulate);
+                            tc_mma_ts(acc1, a0 + 64 + k16 * 8, bd, idesc, accumulate);
                             accumulate = 1;
                         }
                         issued = true;
                         tc_commit(&aempty[ab.idx]);
-                        ab.next(kNumABuf);
+                        ab.next(nabuf);
                     }
                     if (!ok) break;
                     tc_commit(&empty[st.idx]);
@@ -360,6 +398,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         Ring sb;
         const int ng = p.ngroups;
         const int ng_item = ng / ksplit;           // groups of one K split
+        const int rb = ng_item * 2;                // scale bytes of one row for one item
+        const int cb = p.scale_copy_bytes;         // cp.async size (0: plain loads)
         for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
             if (!mbar_wait_bounded(&sempty[sb.idx], sb.phase ^ 1u, abort_flag, status)) break;
             const int u = v / ksplit;
@@ -367,13 +407,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int4 tile = p.tiles[u / p.mt_count];
             int r0, r1;
             unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
-            uint16_t* dst = sS + sb.idx * (ng * 2 * kRowsPerTile);
-            for (int r = lane; r < 2 * kRowsPerTile; r += 32) {
-                const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
-                const uint16_t* src = p.scales + static_cast<int64_t>(grow) * ng + g0;
-                for (int g = 0; g < ng_item; ++g) dst[g * 2 * kRowsPerTile + r] = __ldg(src + g);
+            // buffer layout [256 rows][ng_item] fp16
+            uint8_t* dst = reinterpret_cast<uint8_t*>(sS + sb.idx * (ng * 2 * kRowsPerTile));
+            if (cb) {
+                const int cpr = rb / cb;           // copies per row
+                for (int i = lane; i < 2 * kRowsPerTile * cpr; i += 32) {
+                    const int r = i / cpr;
+                    const int c = i - r * cpr;
+                    const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
+                    const uint8_t* src =
+                        reinterpret_cast<const uint8_t*>(p.scales + static_cast<int64_t>(grow) * ng + g0) + c * cb;
+                    uint8_t* d = dst + r * rb + c * cb;
+                    if (cb == 16)
+                        cp_async<16>(d, src);
+                    else if (cb == 8)
+                        cp_async<8>(d, src);
+                    else
+                        cp_async<4>(d, src);
+                }
+                cp_async_arrive(&sfull[sb.idx]);
+            } else {
+                uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
+                for (int r = lane; r < 2 * kRowsPerTile; r += 32) {
+                    const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
+                    const uint16_t* src = p.scales + static_cast<int64_t>(grow) * ng + g0;
+                    for (int g = 0; g < ng_item; ++g) d16[r * ng_item + g] = __ldg(src + g);
+                }
+                mbar_arrive(&sfull[sb.idx]);
             }
-            mbar_arrive(&sfull[sb.idx]);
             sb.next(2);
         }
     } else if (warp >= 4) {
@@ -383,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quarter * 32 + lane;    // row within the block
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t xr = static_cast<uint32_t>((row * pitch) >> 7) & static_cast<uint32_t>(pitch / 16 - 1);
-        const uint32_t abase = tmem + static_cast<uint32_t>(2 * nt) + lane_base + static_cast<uint32_t>(blk * 32);
+        const uint32_t abase = tmem + static_cast<uint32_t>(2 * nt) + lane_base + static_cast<uint32_t>(blk * 64);
         const float L = p.limit;
         Ring st, ab, sb;
         uint32_t accphase = 0, splitphase = 0;
@@ -395,30 +456,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int4 tile = p.tiles[u / p.mt_count];
             const int mt = u % p.mt_count;
             if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
-            const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + blk * kRowsPerTile + row;
+            const int ng_item = p.ngroups / ksplit;
+            const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + (blk * kRowsPerTile + row) * ng_item;
             for (int ks = split * kps; ks < (split + 1) * kps && ok; ++ks) {
-                if (!mbar_wait_bounded(&full[st.idx], st.phase, abort_flag, status)) {
+                if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
                     ok = false;
                     break;
                 }
                 const uint8_t* wrow = sW + st.idx * 2 * w_tile_bytes + blk * w_tile_bytes + row * pitch;
                 for (int c = 0; c < chunks; ++c) {
-                    const int k0 = ks * kp + c * kKA;
-                    const float s =
-                        __half2float(__ushort_as_half(srow[((k0 - kbeg) / p.group) * 2 * kRowsPerTile]));
-                    uint32_t v[32];
-                    dequant_chunk<BITS>(wrow, xr, c, s, v);
-                    if (!mbar_wait_bounded(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
+                    // one TMEM A buffer = 128 k = two 64-k halves (scales may differ for group 64)
+                    const int k0 = ks * kp + c * kKA - kbeg;
+                    const float s0 = __half2float(__ushort_as_half(srow[k0 / p.group]));
+                    const float s1 = __half2float(__ushort_as_half(srow[(k0 + 64) / p.group]));
+                    uint32_t v0[32], v1[32];
+                    dequant_chunk<BITS>(wrow, xr, 2 * c, s0, v0);
+                    dequant_chunk<BITS>(wrow, xr, 2 * c + 1, s1, v1);
+                    if (!mbar_wait(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    tc_st_32x32b_x32(abase + ab.idx * 64, v);
+                    tc_st_32x32b_x32(abase + ab.idx * 128, v0);
+                    tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v1);
                     tc_wait_st();
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&afull[ab.idx]);
-                    ab.next(kNumABuf);
+                    ab.next(nabuf);
                 }
                 if (!ok) break;
                 __syncwarp();
@@ -439,15 +504,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Split K: park this split's fp32 sums (real token columns only);
                 // the last split of the unit to arrive adds all splits in split
                 // order (deterministic) and runs the epilogue.
-                float* mine = p.partial + static_cast<int64_t>(v) * (2 * kRowsPerTile * nt) +
-                              (blk * kRowsPerTile + row) * nt;
+                // partial[split][mt][permuted row][256 weight rows]: only real token rows
+                const int wrow = blk * kRowsPerTile + row;
+                const int64_t R_rows = p.partial_rows;
+                float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
+                                              (2 * kRowsPerTile) + wrow;
                 for (int j0 = 0; j0 < rows; j0 += 8) {
                     uint32_t d[8];
                     tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(blk * nt + j0), d);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
-                        if (j0 + i < rows) __stcg(mine + j0 + i, __uint_as_float(d[i]));
+                        if (j0 + i < rows) __stcg(mine + (j0 + i) * (2 * kRowsPerTile), __uint_as_float(d[i]));
                 }
                 tc_fence_before();
                 __threadfence();
@@ -471,23 +539,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 splitphase ^= 1u;
                 if (!*last_flag) continue;
                 __threadfence();
-                const float* base = p.partial + static_cast<int64_t>(u) * ksplit * (2 * kRowsPerTile * nt) + row * nt;
-                const int stride = 2 * kRowsPerTile * nt;
+                // stride between splits, and the start of this unit's rows in split 0
+                const int64_t sstride = static_cast<int64_t>(p.mt_count) * R_rows * (2 * kRowsPerTile);
+                const float* base = p.partial + (static_cast<int64_t>(mt) * R_rows + row0) * (2 * kRowsPerTile);
                 if constexpr (W13) {
-                    const int n = mt * kRowsPerTile + row;
+                    const int n0 = mt * kRowsPerTile + row;
+                    const int n = p.h_interleaved ? interleave16(n0) : n0;
                     for (int j = blk; j < rows; j += 2) {
                         float g = 0.f, uu = 0.f;
                         for (int q = 0; q < ksplit; ++q) {
-                            g += __ldcg(base + q * stride + j);
-                            uu += __ldcg(base + q * stride + kRowsPerTile * nt + j);
+                            const float* r = base + q * sstride + j * (2 * kRowsPerTile);
+                            g += __ldcg(r + row);
+                            uu += __ldcg(r + kRowsPerTile + row);
                         }
                         p.out[static_cast<int64_t>(row0 + j) * p.out_ld + n] = __float2bfloat16_rn(swiglu(g, uu, L));
                     }
                 } else {
-                    const int m = mt * 2 * kRowsPerTile + blk * kRowsPerTile + row;
+                    const int m = mt * 2 * kRowsPerTile + wrow;
                     for (int j = 0; j < rows; ++j) {
                         float acc = 0.f;
-                        for (int q = 0; q < ksplit; ++q) acc += __ldcg(base + q * stride + blk * kRowsPerTile * nt + j);
+                        for (int q = 0; q < ksplit; ++q) acc += __ldcg(base + q * sstride + j * (2 * kRowsPerTile) + wrow);
                         p.out[static_cast<int64_t>(row0 + j) * p.out_ld + m] = __float2bfloat16_rn(acc);
                     }
                 }
@@ -497,7 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // both blocks read gate (acc0) and up (acc1) of their lane; block 0
                 // takes the first half of the tokens, block 1 the second half
                 const int half = nt / 2;
-                const int n = mt * kRowsPerTile + row;
+                const int n0 = mt * kRowsPerTile + row;
+                const int n = p.h_interleaved ? interleave16(n0) : n0;
                 for (int j0 = blk * half; j0 < (blk + 1) * half; j0 += 8) {
                     uint32_t g[8], uu[8];
                     tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(j0), g);
@@ -548,7 +620,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
     const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
-    const int bar_bytes = 8 * (2 * 16 + 2 * kNumABuf + 2 + 4 + 3) + 16;
+    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 2 + 4 + 3) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);
     if (ns > 8) ns = 8;
@@ -558,7 +630,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     L.off_w = ns * b_stage;
     L.off_s = L.off_w + ns * w_stage;
     L.off_bar = (L.off_s + s_bytes + 7) & ~7;
-    L.total = L.off_bar + 8 * (2 * ns + 2 * kNumABuf + 2 + 4 + 3) + 16 + 1024;
+    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 2 + 4 + 3) + 16 + 1024;
     return L;
 }
 
@@ -572,8 +644,7 @@ static cudaError_t launch_impl(const CUtensorMap& tm_w, const CUtensorMap& tm_b,
         if (err != cudaSuccess) return err;
         attr_bytes = smem_bytes;
     }
-    kern<<<grid, kThreads, smem_bytes, stream>>>(tm_w, tm_b, p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kThreads), static_cast<size_t>(smem_bytes), stream, tm_w, tm_b, p);
 }
 
 cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, const CUtensorMap& tm_b,

@@ -23,13 +23,17 @@ struct GemmParams {
     int kp;                     // K elements per pipeline stage
     int nt;                     // token tile (MMA N): 16, 32, 64 or 128
     int nstage;                 // smem pipeline depth
+    int nabuf;                  // TMEM A buffers (128 k each)
     int off_b, off_w, off_s, off_bar;   // smem layout (bytes from the 1024-aligned base)
     float limit;                // SwiGLU limit (w13 only)
     int* status;                // device status word
     int ksplit;                 // K splits per unit (1: no split)
-    float* partial;             // split-K partial sums [units * ksplit][2][128][nt] fp32
+    float* partial;             // split-K partial sums [ksplit][mt_count][partial_rows][256] fp32
+    int partial_rows;           // rows of the permuted token order (R)
     int* counters;              // split-K arrival counters [units], zero on entry
     int row_boxes;              // 1: token tiles are loaded one real row at a time
+    int h_interleaved;          // w13: store h columns in the interleaved 16-k order (2-bit w2 input)
+    int scale_copy_bytes;       // 16, 8 or 4: cp.async size for the scale rows; 0: plain loads
 };
 
 struct GemmSmem {
@@ -49,7 +53,11 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, 
                          int* inv, int4* tiles, int* n_tiles, int* status, int* zero, int n_zero,
                          cudaStream_t stream);
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
-                          int K, __nv_bfloat16* xp, cudaStream_t stream);
+                          int K, int interleave, __nv_bfloat16* xp, cudaStream_t stream);
+// dst[i, :] = src[i, :] with every 16-element block in the interleaved K order
+// (0, 8, 1, 9, ..., 7, 15) (or back, with inverse = 1).
+cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
+                                   __nv_bfloat16* dst, cudaStream_t stream);
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
                            __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,

@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     int* cnt = sm;                          // [kRouteWarps][E]
     int* scratch = sm + kRouteWarps * E;    // 64 ints
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();
     if (tid == 0) *status = kStatusOk;
     for (int i = tid; i < n_zero; i += kRouteThreads) zero[i] = 0;   // split-K arrival counters
 
@@ -142,22 +143,71 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
 }
 
-// Xp[i, :] = x[perm[i] / topk, :] for the valid rows i < offsets[E].
+// 16 BF16 (elements 0..15 of a block, as two 8-element vectors) -> the
+// interleaved order (0, 8, 1, 9, ..., 7, 15), and back.
+__device__ __forceinline__ void interleave_block(const uint4& lo, const uint4& hi, uint4& a, uint4& b) {
+    a.x = __byte_perm(lo.x, hi.x, 0x5410);  // lo0 hi0
+    a.y = __byte_perm(lo.x, hi.x, 0x7632);  // lo1 hi1
+    a.z = __byte_perm(lo.y, hi.y, 0x5410);
+    a.w = __byte_perm(lo.y, hi.y, 0x7632);
+    b.x = __byte_perm(lo.z, hi.z, 0x5410);
+    b.y = __byte_perm(lo.z, hi.z, 0x7632);
+    b.z = __byte_perm(lo.w, hi.w, 0x5410);
+    b.w = __byte_perm(lo.w, hi.w, 0x7632);
+}
+__device__ __forceinline__ void deinterleave_block(const uint4& a, const uint4& b, uint4& lo, uint4& hi) {
+    lo.x = __byte_perm(a.x, a.y, 0x5410);
+    hi.x = __byte_perm(a.x, a.y, 0x7632);
+    lo.y = __byte_perm(a.z, a.w, 0x5410);
+    hi.y = __byte_perm(a.z, a.w, 0x7632);
+    lo.z = __byte_perm(b.x, b.y, 0x5410);
+    hi.z = __byte_perm(b.x, b.y, 0x7632);
+    lo.w = __byte_perm(b.z, b.w, 0x5410);
+    hi.w = __byte_perm(b.z, b.w, 0x7632);
+}
+
+// Xp[i, :] = x[perm[i] / topk, :] for the valid rows i < offsets[E]
+// (optionally in the interleaved 16-k order).
 __global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
-                              const int* __restrict__ offsets_end, int topk, int vec_per_row,
+                              const int* __restrict__ offsets_end, int topk, int vec_per_row, int interleave,
                               uint4* __restrict__ xp) {
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x;
     if (i >= *offsets_end) return;
     const int64_t t = perm[i] / topk;
     const uint4* src = x + t * vec_per_row;
     uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
-    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
+    if (!interleave) {
+        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
+    } else {
+        for (int v = 2 * threadIdx.x; v < vec_per_row; v += 2 * blockDim.x) {
+            uint4 a, b;
+            interleave_block(__ldg(src + v), __ldg(src + v + 1), a, b);
+            dst[v] = a;
+            dst[v + 1] = b;
+        }
+    }
+}
+
+__global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t blocks, int inverse,
+                                       uint4* __restrict__ dst) {
+    const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (b >= blocks) return;
+    uint4 a, c;
+    if (inverse)
+        deinterleave_block(src[2 * b], src[2 * b + 1], a, c);
+    else
+        interleave_block(src[2 * b], src[2 * b + 1], a, c);
+    dst[2 * b] = a;
+    dst[2 * b + 1] = c;
 }
 
 // out[t, m] = bf16( sum_j w[t, j] * y[inv[t*topk + j], m] ), fp32, j ascending;
 // a slot whose inverse index is -1 (bad expert id) adds nothing.
 __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restrict__ w, const int* __restrict__ inv,
                                int topk, int vec_per_row, uint4* __restrict__ out) {
+    pdl_wait();
     const int t = blockIdx.y;
     const int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= vec_per_row) return;
@@ -213,12 +263,21 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, 
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
-                          __nv_bfloat16* xp, cudaStream_t stream) {
+                          int interleave, __nv_bfloat16* xp, cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
     const int vpr = K / 8;
     const int threads = vpr >= 256 ? 256 : 32;
-    gather_kernel<<<R, threads, 0, stream>>>(reinterpret_cast<const uint4*>(x), perm, offsets_end, topk, vpr,
-                                             reinterpret_cast<uint4*>(xp));
+    return launch_pdl(gather_kernel, dim3(R), dim3(threads), 0, stream, reinterpret_cast<const uint4*>(x), perm,
+                      offsets_end, topk, vpr, interleave, reinterpret_cast<uint4*>(xp));
+}
+
+cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
+                                   __nv_bfloat16* dst, cudaStream_t stream) {
+    const int64_t blocks = rows * cols / 16;
+    if (blocks == 0) return cudaSuccess;
+    const int threads = 256;
+    interleave_rows_kernel<<<static_cast<unsigned>((blocks + threads - 1) / threads), threads, 0, stream>>>(
+        reinterpret_cast<const uint4*>(src), blocks, inverse, reinterpret_cast<uint4*>(dst));
     return cudaGetLastError();
 }
 
@@ -228,9 +287,8 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const i
     const int vpr = K / 8;
     const int threads = 128;
     dim3 grid((vpr + threads - 1) / threads, T);
-    combine_kernel<<<grid, threads, 0, stream>>>(reinterpret_cast<const uint4*>(y), weights, inv, topk, vpr,
-                                                 reinterpret_cast<uint4*>(out));
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y), weights, inv,
+                      topk, vpr, reinterpret_cast<uint4*>(out));
 }
 
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,

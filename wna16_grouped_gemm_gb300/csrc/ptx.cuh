@@ -3,10 +3,30 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace wna16 {
+
+// Launch `kernel` on `stream` as a programmatic dependent of the previous work
+// in the stream (host side; the kernel must call pdl_wait() before reading
+// anything the previous kernel writes).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Device status word values (mirror wna16_status in include/wna16_moe.h).
 constexpr int kStatusOk = 0;
@@ -28,6 +48,16 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 __device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
+
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until the grids this one depends on (same stream, launched with
+// programmatic serialisation) have completed and their writes are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid in the stream to start launching (its CTAs still wait
+// in pdl_wait() for this grid to complete before reading its output).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -79,6 +109,25 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t pa
             return false;
         }
     }
+}
+
+// ---------------------------------------------------------------- cp.async
+
+// Asynchronous global -> shared copy of 4, 8 or 16 bytes (both addresses aligned to the size).
+template <int BYTES>
+__device__ __forceinline__ void cp_async(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(dst)), "l"(src), "n"(BYTES) : "memory");
+}
+
+// Count one arrival on `bar` when all of this thread's earlier cp.async copies have landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Fast path inline, bounded slow path out of line.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int* status) {
+    if (mbar_try_wait(smem_u32(bar), parity)) return true;
+    return mbar_wait_bounded(bar, parity, abort, status);
 }
 
 // ---------------------------------------------------------------- TMA
