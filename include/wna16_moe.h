@@ -151,6 +151,33 @@ WNA16_API int wna16_moe_combine(const void* y, const float* topk_weights, int64_
                       int64_t E, int64_t N, int bits, void* out, void* workspace,
                       size_t workspace_bytes, void* stream);
 
+/* ---- allocation-free forward (no counterpart on the pages). ----
+ * For callers that cannot allocate device memory while they run: a serving
+ * loop whose device memory is all owned by another allocator, or a
+ * latency-critical path that must not risk cudaMalloc failing or
+ * synchronising the device.  Same arguments and results as
+ * wna16_moe_forward, minus the workspace: the scratch is one fixed 32 MiB
+ * device array inside the library, which every GPU that loads the library
+ * holds until the process exits.  Sizes whose workspace
+ * (wna16_moe_workspace_size) exceeds 32 MiB are rejected with
+ * WNA16_ERR_WORKSPACE_TOO_SMALL and a message, and nothing is launched
+ * (decode batches up to about 160 tokens of hidden 4096 / intermediate 2048 /
+ * 256 experts / top-8 fit).  The call allocates nothing: no cudaMalloc or
+ * cudaFree and no allocating library routine.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture.  Every
+ * call uses the same array and it keeps the previous call's contents (the
+ * forward clears what must start at zero); calls that overlap on the GPU --
+ * on different streams or from different host threads -- race on it, so the
+ * caller must serialise them.  The device status word lives in that shared
+ * array and cannot be read back by the caller. */
+WNA16_API int wna16_moe_forward_noalloc(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                                        const int32_t* w13_packed, const uint16_t* w13_scales,
+                                        const int32_t* w2_packed, const uint16_t* w2_scales,
+                                        int64_t T, int64_t K, int64_t N, int64_t E, int topk,
+                                        int group_size, int group_size_w2, int bits, float swiglu_limit,
+                                        void* out, void* stream);
+
 /* ---- instrumentation (not part of the method): per-stage device times. ----
  * wna16_moe_profile(slots) with slots > 0 makes every later
  * wna16_moe_forward on the calling thread record CUDA events on its stream

@@ -68,6 +68,8 @@ def load_library(path: str = LIB_PATH):
     lib.wna16_moe_w13.argtypes = [P, P, P, P, I64, I64, I64, I64, I, I, I, F, P, P, SZ, P]
     lib.wna16_moe_w2.restype = I
     lib.wna16_moe_w2.argtypes = [P, P, P, I64, I64, I64, I64, I, I, I, P, P, SZ, P]
+    lib.wna16_moe_forward_noalloc.restype = I
+    lib.wna16_moe_forward_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, I, I, F, P, P]
     lib.wna16_moe_profile.restype = I
     lib.wna16_moe_profile.argtypes = [I]
     lib.wna16_moe_profile_read.restype = I
@@ -163,6 +165,30 @@ def forward(x, topk_ids, topk_weights, w13_packed, w13_scales, w2_packed, w2_sca
         _ptr(w2_scales), T, K, N, E, topk, group_size, group_size_w2, bits, float(swiglu_limit), _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc)
+    return out
+
+
+def forward_noalloc(x, topk_ids, topk_weights, w13_packed, w13_scales, w2_packed, w2_scales, *, bits: int,
+                    group_size: int, group_size_w2: int = 0, swiglu_limit: float = 7.0, out=None,
+                    stream=None) -> torch.Tensor:
+    """The forward with the library's static scratch instead of a workspace
+    (for callers that cannot allocate device memory while running); same
+    results as forward().  Calls that overlap on the GPU race on that scratch."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(topk_ids, torch.int32, "topk_ids", 2)
+    _need(topk_weights, torch.float32, "topk_weights", 2)
+    _need(w13_packed, torch.int32, "w13_packed", 3)
+    _need(w2_packed, torch.int32, "w2_packed", 3)
+    _need(w13_scales, torch.float16, "w13_scales", 3)
+    _need(w2_scales, torch.float16, "w2_scales", 3)
+    T, K, N, E, topk = _dims(x, topk_ids, w13_packed, w2_packed, bits)
+    if out is None:
+        out = torch.empty(T, K, dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, "out", 2)
+    _check(load_library().wna16_moe_forward_noalloc(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(w13_packed), _ptr(w13_scales), _ptr(w2_packed),
+        _ptr(w2_scales), T, K, N, E, topk, group_size, group_size_w2, bits, float(swiglu_limit), _ptr(out),
+        _stream(stream)))
     return out
 
 

@@ -354,6 +354,14 @@ int launch_plan(const GemmPlan& P, cudaStream_t s) {
 
 }  // namespace
 
+int wna16::set_error(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
 // ====================================================================== C ABI
 
 extern "C" {

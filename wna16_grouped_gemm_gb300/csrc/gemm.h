@@ -48,6 +48,9 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem);
 cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, const CUtensorMap& tm_b,
                                 const GemmParams& p, int grid, int smem_bytes, cudaStream_t stream);
 
+// Record a host-side error message for wna16_moe_last_error (api.cu); returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 // Routing / gather / combine / pack kernels (kernels.cu).
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
                          int* inv, int4* tiles, int* n_tiles, int* status, int* zero, int n_zero,
