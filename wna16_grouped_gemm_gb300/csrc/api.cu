@@ -316,7 +316,9 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.kp = kp;
     gp.nt = nt;
     gp.nstage = sm.nstage;
-    gp.nabuf = (512 - 2 * nt) / 128 < 3 ? (512 - 2 * nt) / 128 : 3;
+    // TMEM (512 columns): nacc accumulator pairs of 2*nt columns, then A buffers of 128
+    gp.nacc = nt <= 64 ? 2 : 1;
+    gp.nabuf = (512 - gp.nacc * 2 * nt) / 128 < 3 ? (512 - gp.nacc * 2 * nt) / 128 : 3;
     gp.off_b = sm.off_b;
     gp.off_w = sm.off_w;
     gp.off_s = sm.off_s;

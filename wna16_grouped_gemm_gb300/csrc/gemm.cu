@@ -33,7 +33,11 @@ namespace wna16 {
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kFirstDequantWarp = 4;
+constexpr int kDequantWarps = 8;       // 2 per TMEM lane quarter: one per 128-row block
+constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
+constexpr int kEpilogueWarps = 4;      // 1 per TMEM lane quarter
+constexpr int kThreads = 32 * (kFirstEpilogueWarp + kEpilogueWarps);
 constexpr int kRowsPerTile = 128;
 constexpr int kKA = 128;         // K elements per TMEM A buffer (per row block): 64 columns
 constexpr int kMaxABuf = 3;      // TMEM A ring depth (fewer when the accumulators need the columns)
@@ -213,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ksteps = p.kred / kp;
     const int chunks = kp / kKA;
     const int nabuf = p.nabuf;
+    const int nacc = p.nacc;
 
     uint8_t* sB = smem + p.off_b;
     uint8_t* sW = smem + p.off_w;
@@ -222,9 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* empty = full + nstage;
     uint64_t* afull = empty + nstage;
     uint64_t* aempty = afull + kMaxABuf;
-    uint64_t* accfull = aempty + kMaxABuf;
-    uint64_t* accempty = accfull + 1;
-    uint64_t* sfull = accempty + 1;
+    uint64_t* accfull = aempty + kMaxABuf;     // [2]
+    uint64_t* accempty = accfull + 2;          // [2]
+    uint64_t* sfull = accempty + 2;
     uint64_t* sempty = sfull + 2;
     uint64_t* drain = sempty + 2;
     uint64_t* pdone = drain + 1;      // split K: all epilogue warps parked their partial sums
@@ -236,20 +241,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < nstage; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 8 + 1);
+            mbar_init(&empty[i], kDequantWarps + 1);
         }
         for (int i = 0; i < kMaxABuf; ++i) {
-            mbar_init(&afull[i], 8);
+            mbar_init(&afull[i], kDequantWarps);
             mbar_init(&aempty[i], 1);
         }
-        mbar_init(accfull, 1);
-        mbar_init(accempty, 8);
         for (int i = 0; i < 2; ++i) {
+            mbar_init(&accfull[i], 1);
+            mbar_init(&accempty[i], kEpilogueWarps);
             mbar_init(&sfull[i], 32);
-            mbar_init(&sempty[i], 8);
+            mbar_init(&sempty[i], kDequantWarps);
         }
         mbar_init(drain, 1);
-        mbar_init(pdone, 8);
+        mbar_init(pdone, kEpilogueWarps);
         mbar_init(pflag, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -274,6 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_items = n_units * ksplit;         // item = (unit, K split)
     const int kps = ksteps / ksplit;              // stages per item
     int* status = p.status;
+    // TMEM columns: [accumulator pair 0 | pair 1 (decode)] [A buffers]
+    const uint32_t abase_col = static_cast<uint32_t>(nacc * 2 * nt);
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -337,16 +344,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
-            const uint32_t acc0 = tmem;                     // row block 0 accumulator
-            const uint32_t acc1 = tmem + static_cast<uint32_t>(nt);
-            const uint32_t abase = tmem + static_cast<uint32_t>(2 * nt);
-            Ring st, ab;
-            uint32_t accphase = 0;
+            const uint32_t abase = tmem + abase_col;
+            Ring st, ab, acc;
             bool ok = true;
             bool issued = false;
             for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
-                if (!mbar_wait_bounded(accempty, accphase ^ 1u, abort_flag, status)) break;
+                if (!mbar_wait_bounded(&accempty[acc.idx], acc.phase ^ 1u, abort_flag, status)) break;
                 tc_fence_after();
+                const uint32_t acc0 = tmem + acc.idx * 2 * nt;      // row block 0 accumulator
+                const uint32_t acc1 = acc0 + static_cast<uint32_t>(nt);
                 uint32_t accumulate = 0;
                 for (int ks = 0; ks < kps && ok; ++ks) {
                     if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
@@ -380,8 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st.next(nstage);
                 }
                 if (!ok) break;
-                tc_commit(accfull);
-                accphase ^= 1u;
+                tc_commit(&accfull[acc.idx]);
+                acc.next(nacc);
             }
             if (!ok && issued) {
                 // make sure no MMA is still running before TMEM is released
@@ -437,24 +443,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             sb.next(2);
         }
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ dequant + epilogue
-        const int blk = (warp - 4) >> 2;        // row block 0 or 1
-        const int quarter = warp & 3;           // TMEM lanes 32*quarter ..
-        const int row = quarter * 32 + lane;    // row within the block
+    } else if (warp >= kFirstDequantWarp && warp < kFirstDequantWarp + kDequantWarps) {
+        // ------------------------------------------------------------ dequant
+        const int blk = (warp - kFirstDequantWarp) >> 2;   // row block 0 or 1
+        const int quarter = warp & 3;                     // TMEM lanes 32*quarter ..
+        const int row = quarter * 32 + lane;              // row within the block
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t xr = static_cast<uint32_t>((row * pitch) >> 7) & static_cast<uint32_t>(pitch / 16 - 1);
-        const uint32_t abase = tmem + static_cast<uint32_t>(2 * nt) + lane_base + static_cast<uint32_t>(blk * 64);
-        const float L = p.limit;
+        const uint32_t abase = tmem + abase_col + lane_base + static_cast<uint32_t>(blk * 64);
         Ring st, ab, sb;
-        uint32_t accphase = 0, splitphase = 0;
         bool ok = true;
         for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
             const int u = v / ksplit;
             const int split = v - u * ksplit;
             const int kbeg = split * kps * kp;
-            const int4 tile = p.tiles[u / p.mt_count];
-            const int mt = u % p.mt_count;
             if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
             const int ng_item = p.ngroups / ksplit;
             const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + (blk * kRowsPerTile + row) * ng_item;
@@ -465,19 +467,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* wrow = sW + st.idx * 2 * w_tile_bytes + blk * w_tile_bytes + row * pitch;
                 for (int c = 0; c < chunks; ++c) {
-                    // one TMEM A buffer = 128 k = two 64-k halves (scales may differ for group 64)
+                    // one TMEM A buffer = 128 k = two 64-k halves (scales may differ for group 64);
+                    // the first half's TMEM store overlaps the second half's arithmetic
                     const int k0 = ks * kp + c * kKA - kbeg;
                     const float s0 = __half2float(__ushort_as_half(srow[k0 / p.group]));
                     const float s1 = __half2float(__ushort_as_half(srow[(k0 + 64) / p.group]));
                     uint32_t v0[32], v1[32];
                     dequant_chunk<BITS>(wrow, xr, 2 * c, s0, v0);
-                    dequant_chunk<BITS>(wrow, xr, 2 * c + 1, s1, v1);
                     if (!mbar_wait(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     tc_st_32x32b_x32(abase + ab.idx * 128, v0);
+                    dequant_chunk<BITS>(wrow, xr, 2 * c + 1, s1, v1);
                     tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v1);
                     tc_wait_st();
                     tc_fence_before();
@@ -494,38 +497,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sempty[sb.idx]);
             sb.next(2);
-
-            // epilogue
-            if (!mbar_wait_bounded(accfull, accphase, abort_flag, status)) break;
-            tc_fence_after();
+        }
+    } else if (warp >= kFirstEpilogueWarp) {
+        // ------------------------------------------------------------ epilogue
+        // thread = TMEM lane = weight row `row` of both row blocks
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+        const float L = p.limit;
+        Ring acc;
+        uint32_t splitphase = 0;
+        for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+            const int u = v / ksplit;
+            const int split = v - u * ksplit;
+            const int4 tile = p.tiles[u / p.mt_count];
+            const int mt = u % p.mt_count;
             const int rows = tile.z;
             const int row0 = tile.y;
+            if (!mbar_wait_bounded(&accfull[acc.idx], acc.phase, abort_flag, status)) break;
+            tc_fence_after();
+            const uint32_t a0 = tmem + lane_base + acc.idx * 2 * nt;   // block 0 columns; block 1 at + nt
             if (ksplit > 1) {
                 // Split K: park this split's fp32 sums (real token columns only);
                 // the last split of the unit to arrive adds all splits in split
                 // order (deterministic) and runs the epilogue.
-                // partial[split][mt][permuted row][256 weight rows]: only real token rows
-                const int wrow = blk * kRowsPerTile + row;
+                // partial[split][mt][permuted row][256 weight rows]
                 const int64_t R_rows = p.partial_rows;
                 float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
-                                              (2 * kRowsPerTile) + wrow;
+                                              (2 * kRowsPerTile) + row;
                 for (int j0 = 0; j0 < rows; j0 += 8) {
-                    uint32_t d[8];
-                    tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(blk * nt + j0), d);
+                    uint32_t d0[8], d1[8];
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0), d0);
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0), d1);
                     tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (j0 + i < rows) __stcg(mine + (j0 + i) * (2 * kRowsPerTile), __uint_as_float(d[i]));
+                    for (int i = 0; i < 8; ++i) {
+                        if (j0 + i < rows) {
+                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile), __uint_as_float(d0[i]));
+                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile) + kRowsPerTile, __uint_as_float(d1[i]));
+                        }
+                    }
                 }
                 tc_fence_before();
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(accempty);
+                    mbar_arrive(&accempty[acc.idx]);
                     mbar_arrive(pdone);
                 }
-                accphase ^= 1u;
-                if (threadIdx.x == 128) {
+                acc.next(nacc);
+                if (warp == kFirstEpilogueWarp && lane == 0) {
                     if (mbar_wait_bounded(pdone, splitphase, abort_flag, status)) {
                         const int old = atomicAdd(&p.counters[u], 1);
                         *last_flag = (old == ksplit - 1);
@@ -537,43 +558,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (!mbar_wait_bounded(pflag, splitphase, abort_flag, status)) break;
                 splitphase ^= 1u;
-                if (!*last_flag) continue;
+                const int last = *last_flag;
+                __syncwarp();
+                if (!last) continue;
                 __threadfence();
                 // stride between splits, and the start of this unit's rows in split 0
                 const int64_t sstride = static_cast<int64_t>(p.mt_count) * R_rows * (2 * kRowsPerTile);
                 const float* base = p.partial + (static_cast<int64_t>(mt) * R_rows + row0) * (2 * kRowsPerTile);
-                if constexpr (W13) {
-                    const int n0 = mt * kRowsPerTile + row;
-                    const int n = p.h_interleaved ? interleave16(n0) : n0;
-                    for (int j = blk; j < rows; j += 2) {
-                        float g = 0.f, uu = 0.f;
-                        for (int q = 0; q < ksplit; ++q) {
-                            const float* r = base + q * sstride + j * (2 * kRowsPerTile);
-                            g += __ldcg(r + row);
-                            uu += __ldcg(r + kRowsPerTile + row);
-                        }
-                        p.out[static_cast<int64_t>(row0 + j) * p.out_ld + n] = __float2bfloat16_rn(swiglu(g, uu, L));
+                for (int j = 0; j < rows; ++j) {
+                    float a = 0.f, b = 0.f;
+                    for (int q = 0; q < ksplit; ++q) {
+                        const float* r = base + q * sstride + j * (2 * kRowsPerTile);
+                        a += __ldcg(r + row);
+                        b += __ldcg(r + kRowsPerTile + row);
                     }
-                } else {
-                    const int m = mt * 2 * kRowsPerTile + wrow;
-                    for (int j = 0; j < rows; ++j) {
-                        float acc = 0.f;
-                        for (int q = 0; q < ksplit; ++q) acc += __ldcg(base + q * sstride + j * (2 * kRowsPerTile) + wrow);
-                        p.out[static_cast<int64_t>(row0 + j) * p.out_ld + m] = __float2bfloat16_rn(acc);
+                    if constexpr (W13) {
+                        const int n0 = mt * kRowsPerTile + row;
+                        const int n = p.h_interleaved ? interleave16(n0) : n0;
+                        p.out[static_cast<int64_t>(row0 + j) * p.out_ld + n] = __float2bfloat16_rn(swiglu(a, b, L));
+                    } else {
+                        const int m = mt * 2 * kRowsPerTile + row;
+                        __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + j) * p.out_ld + m;
+                        o[0] = __float2bfloat16_rn(a);
+                        o[kRowsPerTile] = __float2bfloat16_rn(b);
                     }
                 }
                 continue;
             }
             if constexpr (W13) {
-                // both blocks read gate (acc0) and up (acc1) of their lane; block 0
-                // takes the first half of the tokens, block 1 the second half
-                const int half = nt / 2;
+                // gate = block 0, up = block 1 of the same lane
                 const int n0 = mt * kRowsPerTile + row;
                 const int n = p.h_interleaved ? interleave16(n0) : n0;
-                for (int j0 = blk * half; j0 < (blk + 1) * half; j0 += 8) {
+                for (int j0 = 0; j0 < rows; j0 += 8) {
                     uint32_t g[8], uu[8];
-                    tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(j0), g);
-                    tc_ld_32x32b_x8(tmem + lane_base + static_cast<uint32_t>(nt + j0), uu);
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0), g);
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0), uu);
                     tc_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -584,23 +603,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else {
-                const int m = mt * 2 * kRowsPerTile + blk * kRowsPerTile + row;
-                const uint32_t acc = tmem + lane_base + static_cast<uint32_t>(blk * nt);
-                for (int j0 = 0; j0 < nt; j0 += 8) {
-                    uint32_t d[8];
-                    tc_ld_32x32b_x8(acc + static_cast<uint32_t>(j0), d);
+                const int m = mt * 2 * kRowsPerTile + row;
+                for (int j0 = 0; j0 < rows; j0 += 8) {
+                    uint32_t d0[8], d1[8];
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0), d0);
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0), d1);
                     tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (j0 + i < rows)
-                            p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + m] =
-                                __float2bfloat16_rn(__uint_as_float(d[i]));
+                    for (int i = 0; i < 8; ++i) {
+                        if (j0 + i < rows) {
+                            __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + j0 + i) * p.out_ld + m;
+                            o[0] = __float2bfloat16_rn(__uint_as_float(d0[i]));
+                            o[kRowsPerTile] = __float2bfloat16_rn(__uint_as_float(d1[i]));
+                        }
+                    }
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(accempty);
-            accphase ^= 1u;
+            if (lane == 0) mbar_arrive(&accempty[acc.idx]);
+            acc.next(nacc);
         }
     }
 
@@ -620,7 +642,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
     const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
-    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 2 + 4 + 3) + 16;
+    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + 3) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);
     if (ns > 8) ns = 8;
@@ -630,7 +652,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     L.off_w = ns * b_stage;
     L.off_s = L.off_w + ns * w_stage;
     L.off_bar = (L.off_s + s_bytes + 7) & ~7;
-    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 2 + 4 + 3) + 16 + 1024;
+    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + 3) + 16 + 1024;
     return L;
 }
 
