@@ -316,9 +316,14 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.kp = kp;
     gp.nt = nt;
     gp.nstage = sm.nstage;
-    // TMEM (512 columns): nacc accumulator pairs of 2*nt columns, then A buffers of 128
-    gp.nacc = nt <= 64 ? 2 : 1;
-    gp.nabuf = (512 - gp.nacc * 2 * nt) / 128 < 3 ? (512 - gp.nacc * 2 * nt) / 128 : 3;
+    // TMEM (512 columns): nacc sets of n_issuers accumulators of nt columns,
+    // then A buffers of 128 columns (2 or 3).  A thread can issue a tcgen05.mma
+    // only every ~110 cycles, so small token tiles use 4 issuers (row block x
+    // buffer parity) and large ones 2 (one per row block).
+    gp.n_issuers = nt <= 32 ? 4 : 2;
+    gp.nacc = 2 * gp.n_issuers * nt + 2 * 128 <= 512 ? 2 : 1;
+    const int acc_cols = gp.nacc * gp.n_issuers * nt;
+    gp.nabuf = (512 - acc_cols) / 128 < 3 ? (512 - acc_cols) / 128 : 3;
     gp.off_b = sm.off_b;
     gp.off_w = sm.off_w;
     gp.off_s = sm.off_s;

@@ -33,11 +33,20 @@ namespace wna16 {
 
 namespace {
 
+// Warp roles (18 warps).
+constexpr int kProducerWarp = 0;       // TMA
+constexpr int kScaleWarp = 1;          // cp.async of the scales
+constexpr int kIssuerWarp0 = 2;        // MMA issuers; warp 2 also owns the TMEM allocation
+constexpr int kIssuerWarp1 = 3;
+constexpr int kAllocWarp = kIssuerWarp0;
 constexpr int kFirstDequantWarp = 4;
 constexpr int kDequantWarps = 8;       // 2 per TMEM lane quarter: one per 128-row block
 constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
 constexpr int kEpilogueWarps = 4;      // 1 per TMEM lane quarter
-constexpr int kThreads = 32 * (kFirstEpilogueWarp + kEpilogueWarps);
+constexpr int kIssuerWarp2 = kFirstEpilogueWarp + kEpilogueWarps;
+constexpr int kIssuerWarp3 = kIssuerWarp2 + 1;
+constexpr int kMaxIssuers = 4;
+constexpr int kThreads = 32 * (kIssuerWarp3 + 1);
 constexpr int kRowsPerTile = 128;
 constexpr int kKA = 128;         // K elements per TMEM A buffer (per row block): 64 columns
 constexpr int kMaxABuf = 3;      // TMEM A ring depth (fewer when the accumulators need the columns)
@@ -218,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int chunks = kp / kKA;
     const int nabuf = p.nabuf;
     const int nacc = p.nacc;
+    const int n_iss = p.n_issuers;
 
     uint8_t* sB = smem + p.off_b;
     uint8_t* sW = smem + p.off_w;
@@ -231,9 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* accempty = accfull + 2;          // [2]
     uint64_t* sfull = accempty + 2;
     uint64_t* sempty = sfull + 2;
-    uint64_t* drain = sempty + 2;
-    uint64_t* pdone = drain + 1;      // split K: all epilogue warps parked their partial sums
-    uint64_t* pflag = pdone + 1;      // split K: arrival counted, last_flag is valid
+    uint64_t* drain = sempty + 2;              // [kMaxIssuers]
+    uint64_t* pdone = drain + kMaxIssuers;     // split K: all epilogue warps parked their partial sums
+    uint64_t* pflag = pdone + 1;               // split K: arrival counted, last_flag is valid
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pflag + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
@@ -241,19 +251,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < nstage; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kDequantWarps + 1);
+            mbar_init(&empty[i], kDequantWarps + n_iss);
         }
         for (int i = 0; i < kMaxABuf; ++i) {
             mbar_init(&afull[i], kDequantWarps);
-            mbar_init(&aempty[i], 1);
+            mbar_init(&aempty[i], 2);              // the two issuers (row blocks) that read it
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&accfull[i], 1);
+            mbar_init(&accfull[i], n_iss);
             mbar_init(&accempty[i], kEpilogueWarps);
             mbar_init(&sfull[i], 32);
             mbar_init(&sempty[i], kDequantWarps);
         }
-        mbar_init(drain, 1);
+        for (int i = 0; i < kMaxIssuers; ++i) mbar_init(&drain[i], 1);
         mbar_init(pdone, kEpilogueWarps);
         mbar_init(pflag, 1);
         *abort_flag = 0;
@@ -261,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tm_w);
         tma_prefetch_desc(&tm_b);
     }
-    if (warp == 1) {
+    if (warp == kAllocWarp) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
@@ -278,11 +288,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ksplit = p.ksplit;
     const int n_items = n_units * ksplit;         // item = (unit, K split)
     const int kps = ksteps / ksplit;              // stages per item
+    const int nbuf_item = kps * chunks;           // TMEM A buffers per item
     int* status = p.status;
-    // TMEM columns: [accumulator pair 0 | pair 1 (decode)] [A buffers]
-    const uint32_t abase_col = static_cast<uint32_t>(nacc * 2 * nt);
+    // TMEM columns: [nacc sets x n_iss accumulators of nt columns] [A buffers of 128 columns]
+    const uint32_t acc_set_cols = static_cast<uint32_t>(n_iss * nt);
+    const uint32_t abase_col = static_cast<uint32_t>(nacc) * acc_set_cols;
+    const int issuer = warp == kIssuerWarp0 ? 0 : warp == kIssuerWarp1 ? 1 : warp == kIssuerWarp2 ? 2
+                                                                       : warp == kIssuerWarp3 ? 3 : -1;
 
-    if (warp == 0) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();
@@ -301,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tx_item =
                     p.row_boxes ? static_cast<uint32_t>(2 * w_tile_bytes + (kp / 64) * tile.z * 128) : tx;
                 for (int ks = split * kps; ks < (split + 1) * kps; ++ks) {
-                    if (!mbar_wait(&empty[st.idx], st.phase ^ 1u, abort_flag, status)) {
+                    if (!mbar_try_wait(smem_u32(&empty[st.idx]), st.phase ^ 1u) &&
+                        !mbar_wait_bounded(&empty[st.idx], st.phase ^ 1u, abort_flag, status, true)) {
                         ok = false;
                         break;
                     }
@@ -340,45 +355,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+    } else if (issuer >= 0) {
+        // ------------------------------------------------------------ MMA issuers
+        // Issuer i owns accumulator i of each set: row block t = i & 1; with 4
+        // issuers, parity h = i >> 1 takes the item's A buffers b with b % 2 == h.
+        // One thread can issue a tcgen05.mma only every ~110 cycles, so several
+        // issuers keep the tensor pipe fed.
+        if (lane == 0 && issuer < n_iss) {
+            const int t = issuer & 1;
+            const int h = issuer >> 1;
             const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
-            const uint32_t abase = tmem + abase_col;
             Ring st, ab, acc;
             bool ok = true;
             bool issued = false;
             for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
                 if (!mbar_wait_bounded(&accempty[acc.idx], acc.phase ^ 1u, abort_flag, status)) break;
                 tc_fence_after();
-                const uint32_t acc0 = tmem + acc.idx * 2 * nt;      // row block 0 accumulator
-                const uint32_t acc1 = acc0 + static_cast<uint32_t>(nt);
+                const uint32_t d = tmem + acc.idx * acc_set_cols + static_cast<uint32_t>(issuer * nt);
                 uint32_t accumulate = 0;
+                int bl = 0;   // A buffer index within the item
                 for (int ks = 0; ks < kps && ok; ++ks) {
                     if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t bstage = smem_u32(sB + st.idx * b_stage_bytes);
-                    for (int c = 0; c < chunks; ++c) {
-                        if (!mbar_wait(&afull[ab.idx], ab.phase, abort_flag, status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t a0 = abase + ab.idx * 128;
+                    for (int c = 0; c < chunks; ++c, ++bl) {
+                        if (n_iss == 2 || (bl & 1) == h) {
+                            if (!mbar_wait(&afull[ab.idx], ab.phase, abort_flag, status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t a0 = tmem + abase_col + ab.idx * 128 + t * 64;
 #pragma unroll
-                        for (int k16 = 0; k16 < 8; ++k16) {
-                            // B: 64-k swizzle atom (2c + k16/4), 32 B per 16 k inside it
-                            const uint32_t batom =
-                                bstage + static_cast<uint32_t>((2 * c + (k16 >> 2)) * nt * 128 + (k16 & 3) * 32);
-                            const uint64_t bd = smem_desc_sw128(batom);
-                            tc_mma_ts(acc0, a0 + k16 * 8, bd, idesc, accumulate);
-                            tc_mma_ts(acc1, a0 + 64 + k16 * 8, bd, idesc, accumulate);
-                            accumulate = 1;
+                            for (int k16 = 0; k16 < 8; ++k16) {
+                                // B: 64-k swizzle atom (2c + k16/4), 32 B per 16 k inside it
+                                const uint32_t batom = bstage + static_cast<uint32_t>((2 * c + (k16 >> 2)) * nt * 128 +
+                                                                                      (k16 & 3) * 32);
+                                tc_mma_ts(d, a0 + k16 * 8, smem_desc_sw128(batom), idesc, accumulate);
+                                accumulate = 1;
+                            }
+                            issued = true;
+                            tc_commit(&aempty[ab.idx]);
                         }
-                        issued = true;
-                        tc_commit(&aempty[ab.idx]);
                         ab.next(nabuf);
                     }
                     if (!ok) break;
@@ -390,16 +410,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc.next(nacc);
             }
             if (!ok && issued) {
-                // make sure no MMA is still running before TMEM is released
-                tc_commit(drain);
-                const uint32_t a = smem_u32(drain);
+                // make sure no MMA of this issuer is still running before TMEM is released
+                tc_commit(&drain[issuer]);
+                const uint32_t a = smem_u32(&drain[issuer]);
                 const uint64_t t0 = globaltimer_ns();
                 while (!mbar_try_wait(a, 0)) {
                     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
                 }
             }
         }
-    } else if (warp == 2) {
+    } else if (warp == kScaleWarp) {
         // ------------------------------------------------------------ scale loader
         Ring sb;
         const int ng = p.ngroups;
@@ -407,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rb = ng_item * 2;                // scale bytes of one row for one item
         const int cb = p.scale_copy_bytes;         // cp.async size (0: plain loads)
         for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
-            if (!mbar_wait_bounded(&sempty[sb.idx], sb.phase ^ 1u, abort_flag, status)) break;
+            if (!mbar_wait_bounded(&sempty[sb.idx], sb.phase ^ 1u, abort_flag, status, true)) break;
             const int u = v / ksplit;
             const int g0 = (v - u * ksplit) * ng_item;
             const int4 tile = p.tiles[u / p.mt_count];
@@ -423,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
                     const uint8_t* src =
                         reinterpret_cast<const uint8_t*>(p.scales + static_cast<int64_t>(grow) * ng + g0) + c * cb;
-                    uint8_t* d = dst + r * rb + c * cb;
+                    uint8_t* dd = dst + r * rb + c * cb;
                     if (cb == 16)
-                        cp_async<16>(d, src);
+                        cp_async<16>(dd, src);
                     else if (cb == 8)
-                        cp_async<8>(d, src);
+                        cp_async<8>(dd, src);
                     else
-                        cp_async<4>(d, src);
+                        cp_async<4>(dd, src);
                 }
                 cp_async_arrive(&sfull[sb.idx]);
             } else {
@@ -467,21 +487,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* wrow = sW + st.idx * 2 * w_tile_bytes + blk * w_tile_bytes + row * pitch;
                 for (int c = 0; c < chunks; ++c) {
-                    // one TMEM A buffer = 128 k = two 64-k halves (scales may differ for group 64);
-                    // the first half's TMEM store overlaps the second half's arithmetic
+                    // one TMEM A buffer = 128 k, stored as two 64-k halves (scales
+                    // may differ for group 64); the first store overlaps the second
+                    // half's arithmetic only through the other warps on the scheduler
                     const int k0 = ks * kp + c * kKA - kbeg;
-                    const float s0 = __half2float(__ushort_as_half(srow[k0 / p.group]));
-                    const float s1 = __half2float(__ushort_as_half(srow[(k0 + 64) / p.group]));
-                    uint32_t v0[32], v1[32];
-                    dequant_chunk<BITS>(wrow, xr, 2 * c, s0, v0);
+                    uint32_t v32[32];
+                    dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[k0 / p.group])), v32);
                     if (!mbar_wait(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    tc_st_32x32b_x32(abase + ab.idx * 128, v0);
-                    dequant_chunk<BITS>(wrow, xr, 2 * c + 1, s1, v1);
-                    tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v1);
+                    tc_st_32x32b_x32(abase + ab.idx * 128, v32);
+                    tc_wait_st();
+                    dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[(k0 + 64) / p.group])),
+                                        v32);
+                    tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v32);
                     tc_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -498,13 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&sempty[sb.idx]);
             sb.next(2);
         }
-    } else if (warp >= kFirstEpilogueWarp) {
+    } else if (warp >= kFirstEpilogueWarp && warp < kFirstEpilogueWarp + kEpilogueWarps) {
         // ------------------------------------------------------------ epilogue
-        // thread = TMEM lane = weight row `row` of both row blocks
+        // thread = TMEM lane = weight row `row` of both row blocks; a row
+        // block's sum is its issuers' accumulators added (one or two parities)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const float L = p.limit;
+        const int nh = (n_iss == 4 && nbuf_item >= 2) ? 2 : 1;
         Ring acc;
         uint32_t splitphase = 0;
         for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
@@ -514,9 +537,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int mt = u % p.mt_count;
             const int rows = tile.z;
             const int row0 = tile.y;
-            if (!mbar_wait_bounded(&accfull[acc.idx], acc.phase, abort_flag, status)) break;
+            if (!mbar_wait_bounded(&accfull[acc.idx], acc.phase, abort_flag, status, true)) break;
             tc_fence_after();
-            const uint32_t a0 = tmem + lane_base + acc.idx * 2 * nt;   // block 0 columns; block 1 at + nt
+            const uint32_t a0 = tmem + lane_base + acc.idx * acc_set_cols;   // issuer i at + i * nt
+            // sums of both row blocks for token columns j0..j0+7
+            auto load8 = [&](int j0, float (&s0)[8], float (&s1)[8]) {
+                uint32_t d[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s0[i] = s1[i] = 0.f;
+                for (int hh = 0; hh < nh; ++hh) {
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>((2 * hh) * nt + j0), d);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) s0[i] += __uint_as_float(d[i]);
+                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>((2 * hh + 1) * nt + j0), d);
+                    tc_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) s1[i] += __uint_as_float(d[i]);
+                }
+            };
             if (ksplit > 1) {
                 // Split K: park this split's fp32 sums (real token columns only);
                 // the last split of the unit to arrive adds all splits in split
@@ -526,15 +565,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
                                               (2 * kRowsPerTile) + row;
                 for (int j0 = 0; j0 < rows; j0 += 8) {
-                    uint32_t d0[8], d1[8];
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0), d0);
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0), d1);
-                    tc_wait_ld();
+                    float s0[8], s1[8];
+                    load8(j0, s0, s1);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (j0 + i < rows) {
-                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile), __uint_as_float(d0[i]));
-                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile) + kRowsPerTile, __uint_as_float(d1[i]));
+                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile), s0[i]);
+                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile) + kRowsPerTile, s1[i]);
                         }
                     }
                 }
@@ -590,31 +627,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int n0 = mt * kRowsPerTile + row;
                 const int n = p.h_interleaved ? interleave16(n0) : n0;
                 for (int j0 = 0; j0 < rows; j0 += 8) {
-                    uint32_t g[8], uu[8];
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0), g);
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0), uu);
-                    tc_wait_ld();
+                    float g[8], uu[8];
+                    load8(j0, g, uu);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        if (j0 + i < rows) {
-                            const float hv = swiglu(__uint_as_float(g[i]), __uint_as_float(uu[i]), L);
-                            p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + n] = __float2bfloat16_rn(hv);
-                        }
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        if (j0 + i < rows)
+                            p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + n] =
+                                __float2bfloat16_rn(swiglu(g[i], uu[i], L));
                 }
             } else {
                 const int m = mt * 2 * kRowsPerTile + row;
                 for (int j0 = 0; j0 < rows; j0 += 8) {
-                    uint32_t d0[8], d1[8];
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0), d0);
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0), d1);
-                    tc_wait_ld();
+                    float y0[8], y1[8];
+                    load8(j0, y0, y1);
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (j0 + i < rows) {
                             __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + j0 + i) * p.out_ld + m;
-                            o[0] = __float2bfloat16_rn(__uint_as_float(d0[i]));
-                            o[kRowsPerTile] = __float2bfloat16_rn(__uint_as_float(d1[i]));
+                            o[0] = __float2bfloat16_rn(y0[i]);
+                            o[kRowsPerTile] = __float2bfloat16_rn(y1[i]);
                         }
                     }
                 }
@@ -628,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kAllocWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -642,7 +673,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
     const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
-    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + 3) + 16;
+    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);
     if (ns > 8) ns = 8;
@@ -652,7 +683,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     L.off_w = ns * b_stage;
     L.off_s = L.off_w + ns * w_stage;
     L.off_bar = (L.off_s + s_bytes + 7) & ~7;
-    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + 3) + 16 + 1024;
+    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2) + 16 + 1024;
     return L;
 }
 

@@ -24,7 +24,8 @@ struct GemmParams {
     int nt;                     // token tile (MMA N): 16, 32, 64 or 128
     int nstage;                 // smem pipeline depth
     int nabuf;                  // TMEM A buffers (128 k each)
-    int nacc;                   // TMEM accumulator pairs (2: the epilogue overlaps the next item)
+    int nacc;                   // TMEM accumulator sets (2: the epilogue overlaps the next item)
+    int n_issuers;              // MMA-issuing threads (2 or 4), each with its own accumulator
     int off_b, off_w, off_s, off_bar;   // smem layout (bytes from the 1024-aligned base)
     float limit;                // SwiGLU limit (w13 only)
     int* status;                // device status word

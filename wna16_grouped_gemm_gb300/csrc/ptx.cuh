@@ -91,17 +91,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same, but the thread may sleep in the barrier (up to the hint) until the
+// phase completes, instead of returning at once: waiting warps then take no
+// issue slots from the warps doing the arithmetic.
+constexpr uint32_t kSuspendHintNs = 1000000;  // 1 ms upper bound per call
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) when *abort is set by another thread of the CTA, or after
-// kWaitLimitNs, in which case it sets *abort and the status word.
+// kWaitLimitNs, in which case it sets *abort and the status word.  With
+// `backoff`, the waiter sleeps briefly between polls so that it does not take
+// issue slots from the warps doing the arithmetic.
 static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                               int* status) {
+                                                      int* status, bool backoff = false) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+        for (int i = 0; i < 8; ++i) {
+            if (mbar_try_wait_sleep(a, parity)) return true;
+            if (backoff) __nanosleep(128);
+        }
         if (*abort) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort = 1;
