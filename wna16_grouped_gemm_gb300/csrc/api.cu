@@ -95,7 +95,7 @@ struct Layout {
     int64_t max_tiles = 0;
     int64_t units13 = 0, units2 = 0;      // largest possible unit counts of the two GEMMs
     size_t status = 0, n_tiles = 0, counts = 0, offsets = 0, perm = 0, inv = 0, tiles = 0, xp = 0, h = 0, y = 0;
-    size_t counters13 = 0, counters2 = 0, partial = 0;
+    size_t partial = 0;
     size_t total = 0;
 };
 
@@ -124,8 +124,6 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.xp = o;       o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
     L.h = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * N);
     L.y = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
-    L.counters13 = o; o = align_up(o + sizeof(int) * L.units13);
-    L.counters2 = o;  o = align_up(o + sizeof(int) * L.units2);
     L.partial = o;  o = align_up(o + sizeof(float) * partial_floats);
     L.total = o;
     return L;
@@ -190,18 +188,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D row-major tensor [rows, cols] of `elem`-byte elements, box [box_rows, box_cols].
-int encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, int elem, const void* base, uint64_t rows,
-              uint64_t cols, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle swz) {
+// 3-D tensor: dims[0] contiguous elements; dims[1], dims[2] with byte strides s1, s2.
+int encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, const uint64_t (&dims)[3],
+              const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swz) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return fail(WNA16_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-    cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * static_cast<uint64_t>(elem)};
-    cuuint32_t box[2] = {box_cols, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return fail(WNA16_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    cuuint64_t st[2] = {strides[0], strides[1]};
+    cuuint32_t b[3] = {box[0], box[1], box[2]};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(map, dtype, 3, const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(WNA16_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", static_cast<int>(r));
     return WNA16_OK;
 }
 
@@ -257,8 +255,7 @@ int check_workspace(const void* ws, size_t bytes, const Layout& L) {
 int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStream_t s) {
     cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), L.nt, at<int>(ws, L.counts),
                                  at<int>(ws, L.offsets), at<int>(ws, L.perm), at<int>(ws, L.inv),
-                                 at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status),
-                                 at<int>(ws, L.counters13), static_cast<int>((L.partial - L.counters13) / sizeof(int)), s);
+                                 at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status), s);
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "route kernel launch");
 }
 
@@ -286,20 +283,34 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     const int pitch = kp * bits / 8;
     const int64_t max_units = w13 ? L.units13 : L.units2;
     const int ksplit = choose_split(max_units, kred, kp, group);
-    const bool row_boxes = nt <= 32;
     const int ngroups = static_cast<int>(kred / group);
     GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups, dev.max_smem);
     if (sm.nstage < 2) return fail(WNA16_ERR_UNSUPPORTED, "shared-memory plan does not fit");
 
     const int p = 32 / bits;
-    if (int rc = encode_2d(&P.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, wpacked,
-                           static_cast<uint64_t>(E * rows_per_expert), static_cast<uint64_t>(kred / p), 128,
-                           static_cast<uint32_t>(pitch / 4), swizzle_for_pitch(pitch)))
-        return rc;
-    if (int rc = encode_2d(&P.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b_src, static_cast<uint64_t>(L.R),
-                           static_cast<uint64_t>(kred), row_boxes ? 1u : static_cast<uint32_t>(nt), 64,
-                           CU_TENSOR_MAP_SWIZZLE_128B))
-        return rc;
+    {
+        // weights: [words of a row][rows][the unit's two 128-row blocks], the
+        // second block N rows (w13: up) or 128 rows (w2) after the first
+        const uint64_t row_bytes = static_cast<uint64_t>(kred / p) * 4;
+        const uint64_t block_rows = w13 ? static_cast<uint64_t>(N) : 128;
+        const uint64_t dims[3] = {static_cast<uint64_t>(kred / p),
+                                  static_cast<uint64_t>(E * rows_per_expert) - block_rows, 2};
+        const uint64_t strides[2] = {row_bytes, block_rows * row_bytes};
+        const uint32_t box[3] = {static_cast<uint32_t>(pitch / 4), 128, 2};
+        if (int rc = encode_3d(&P.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, wpacked, dims, strides, box,
+                               swizzle_for_pitch(pitch)))
+            return rc;
+    }
+    {
+        // token rows: [64 elements][rows][64-k atoms] so that one box is the
+        // stage's atoms one after another, each nt rows x 128 B (128B-swizzled)
+        const uint64_t dims[3] = {64, static_cast<uint64_t>(L.R), static_cast<uint64_t>(kred / 64)};
+        const uint64_t strides[2] = {static_cast<uint64_t>(kred) * 2, 128};
+        const uint32_t box[3] = {64, static_cast<uint32_t>(nt), static_cast<uint32_t>(kp / 64)};
+        if (int rc = encode_3d(&P.tm_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, b_src, dims, strides, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B))
+            return rc;
+    }
 
     GemmParams& gp = P.gp;
     gp.tiles = at<const int4>(ws, L.tiles);
@@ -333,8 +344,6 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.ksplit = ksplit;
     gp.partial = ksplit > 1 ? at<float>(ws, L.partial) : nullptr;
     gp.partial_rows = static_cast<int>(L.R);
-    gp.counters = at<int>(ws, w13 ? L.counters13 : L.counters2);
-    gp.row_boxes = row_boxes ? 1 : 0;
     gp.h_interleaved = h_interleaved ? 1 : 0;
     // widest async copy that divides the scale row stride, one split's row
     // segment and the base alignment
@@ -449,11 +458,22 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     mark(2, s);
     if (int rc = launch_plan(p13, s)) return rc;
+    if (p13.gp.ksplit > 1) {   // split K: fixed-order sum of the splits + SwiGLU -> h
+        e = launch_finalize_w13(at<float>(workspace, L.partial), p13.gp.ksplit, static_cast<int>(L.R),
+                                at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, il ? 1 : 0,
+                                at<__nv_bfloat16>(workspace, L.h), s);
+        if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
+    }
     mark(3, s);
     if (int rc = launch_plan(p2, s)) return rc;
     mark(4, s);
-    e = launch_combine(at<__nv_bfloat16>(workspace, L.y), topk_weights, at<int>(workspace, L.inv),
-                       static_cast<int>(T), topk, static_cast<int>(K), static_cast<__nv_bfloat16*>(out), s);
+    if (p2.gp.ksplit > 1)      // split K: the combine adds the splits itself
+        e = launch_combine_partials(at<float>(workspace, L.partial), p2.gp.ksplit, static_cast<int>(L.R), topk_weights,
+                                    at<int>(workspace, L.inv), static_cast<int>(T), topk, static_cast<int>(K),
+                                    static_cast<__nv_bfloat16*>(out), s);
+    else
+        e = launch_combine(at<__nv_bfloat16>(workspace, L.y), topk_weights, at<int>(workspace, L.inv),
+                           static_cast<int>(T), topk, static_cast<int>(K), static_cast<__nv_bfloat16*>(out), s);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     mark(5, s);
     mark_done();
@@ -556,7 +576,14 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
                                   static_cast<int>(K), bits == 2 ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
-    return launch_plan(p13, s);
+    if (int rc = launch_plan(p13, s)) return rc;
+    if (p13.gp.ksplit > 1) {
+        e = launch_finalize_w13(at<float>(workspace, L.partial), p13.gp.ksplit, static_cast<int>(L.R),
+                                at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, 0,
+                                static_cast<__nv_bfloat16*>(h_out), s);
+        if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
+    }
+    return WNA16_OK;
 }
 
 int wna16_moe_w2(const void* h, const int32_t* w2_packed, const uint16_t* w2_scales, int64_t T, int64_t K, int64_t N,
@@ -584,7 +611,14 @@ int wna16_moe_w2(const void* h, const int32_t* w2_packed, const uint16_t* w2_sca
     if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, b_src, y_out, K, N, E, group_size_w2, INFINITY, L,
                            workspace))
         return rc;
-    return launch_plan(p2, s);
+    if (int rc = launch_plan(p2, s)) return rc;
+    if (p2.gp.ksplit > 1) {
+        cudaError_t e = launch_finalize_w2(at<float>(workspace, L.partial), p2.gp.ksplit, static_cast<int>(L.R),
+                                           at<int>(workspace, L.offsets) + E, static_cast<int>(K),
+                                           static_cast<__nv_bfloat16*>(y_out), s);
+        if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
+    }
+    return WNA16_OK;
 }
 
 int wna16_moe_combine(const void* y, const float* topk_weights, int64_t T, int64_t K, int topk, int64_t E, int64_t N,

@@ -242,11 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* sfull = accempty + 2;
     uint64_t* sempty = sfull + 2;
     uint64_t* drain = sempty + 2;              // [kMaxIssuers]
-    uint64_t* pdone = drain + kMaxIssuers;     // split K: all epilogue warps parked their partial sums
-    uint64_t* pflag = pdone + 1;               // split K: arrival counted, last_flag is valid
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(pflag + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < nstage; ++i) {
@@ -264,8 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sempty[i], kDequantWarps);
         }
         for (int i = 0; i < kMaxIssuers; ++i) mbar_init(&drain[i], 1);
-        mbar_init(pdone, kEpilogueWarps);
-        mbar_init(pflag, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_w);
@@ -311,30 +306,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int4 tile = p.tiles[u / p.mt_count];
                 int r0, r1;
                 unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
-                // decode tiles: only the tile's real rows are fetched, one row per box
-                const uint32_t tx_item =
-                    p.row_boxes ? static_cast<uint32_t>(2 * w_tile_bytes + (kp / 64) * tile.z * 128) : tx;
                 for (int ks = split * kps; ks < (split + 1) * kps; ++ks) {
                     if (!mbar_try_wait(smem_u32(&empty[st.idx]), st.phase ^ 1u) &&
                         !mbar_wait_bounded(&empty[st.idx], st.phase ^ 1u, abort_flag, status, true)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[st.idx], tx_item);
-                    uint8_t* w = sW + st.idx * 2 * w_tile_bytes;
-                    const int wc = ks * (kp / kCodes);
-                    tma_load_2d(w, &tm_w, &full[st.idx], wc, r0, pol_w);
-                    tma_load_2d(w + w_tile_bytes, &tm_w, &full[st.idx], wc, r1, pol_w);
-                    uint8_t* b = sB + st.idx * b_stage_bytes;
-                    if (p.row_boxes) {
-                        for (int a = 0; a < kp / 64; ++a)
-                            for (int r = 0; r < tile.z; ++r)
-                                tma_load_2d(b + a * nt * 128 + r * 128, &tm_b, &full[st.idx], ks * kp + a * 64,
-                                            tile.y + r, pol_b);
-                    } else {
-                        for (int a = 0; a < kp / 64; ++a)
-                            tma_load_2d(b + a * nt * 128, &tm_b, &full[st.idx], ks * kp + a * 64, tile.y, pol_b);
-                    }
+                    // two TMA instructions per stage: both weight row blocks in one
+                    // 3-D box, all 64-k atoms of the token tile in another
+                    mbar_arrive_expect_tx(&full[st.idx], tx);
+                    tma_load_3d(sW + st.idx * 2 * w_tile_bytes, &tm_w, &full[st.idx], ks * (kp / kCodes), r0, 0,
+                                pol_w);
+                    tma_load_3d(sB + st.idx * b_stage_bytes, &tm_b, &full[st.idx], 0, tile.y, ks * (kp / 64), pol_b);
                     issued |= 1u << st.idx;
                     last_parity = (last_parity & ~(1u << st.idx)) | (st.phase << st.idx);
                     st.next(nstage);
@@ -529,7 +512,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float L = p.limit;
         const int nh = (n_iss == 4 && nbuf_item >= 2) ? 2 : 1;
         Ring acc;
-        uint32_t splitphase = 0;
         for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
             const int u = v / ksplit;
             const int split = v - u * ksplit;
@@ -557,10 +539,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
             if (ksplit > 1) {
-                // Split K: park this split's fp32 sums (real token columns only);
-                // the last split of the unit to arrive adds all splits in split
-                // order (deterministic) and runs the epilogue.
-                // partial[split][mt][permuted row][256 weight rows]
+                // Split K: park this split's fp32 sums for the tile's real token
+                // rows in partial[split][mt][permuted row][256 weight rows]; a
+                // separate kernel adds the splits in split order (deterministic)
+                // and applies the epilogue.
                 const int64_t R_rows = p.partial_rows;
                 float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
                                               (2 * kRowsPerTile) + row;
@@ -570,56 +552,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (j0 + i < rows) {
-                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile), s0[i]);
-                            __stcg(mine + (j0 + i) * (2 * kRowsPerTile) + kRowsPerTile, s1[i]);
+                            mine[(j0 + i) * (2 * kRowsPerTile)] = s0[i];
+                            mine[(j0 + i) * (2 * kRowsPerTile) + kRowsPerTile] = s1[i];
                         }
                     }
                 }
                 tc_fence_before();
-                __threadfence();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&accempty[acc.idx]);
-                    mbar_arrive(pdone);
-                }
+                if (lane == 0) mbar_arrive(&accempty[acc.idx]);
                 acc.next(nacc);
-                if (warp == kFirstEpilogueWarp && lane == 0) {
-                    if (mbar_wait_bounded(pdone, splitphase, abort_flag, status)) {
-                        const int old = atomicAdd(&p.counters[u], 1);
-                        *last_flag = (old == ksplit - 1);
-                        if (old == ksplit - 1) p.counters[u] = 0;
-                    } else {
-                        *last_flag = 0;
-                    }
-                    mbar_arrive(pflag);
-                }
-                if (!mbar_wait_bounded(pflag, splitphase, abort_flag, status)) break;
-                splitphase ^= 1u;
-                const int last = *last_flag;
-                __syncwarp();
-                if (!last) continue;
-                __threadfence();
-                // stride between splits, and the start of this unit's rows in split 0
-                const int64_t sstride = static_cast<int64_t>(p.mt_count) * R_rows * (2 * kRowsPerTile);
-                const float* base = p.partial + (static_cast<int64_t>(mt) * R_rows + row0) * (2 * kRowsPerTile);
-                for (int j = 0; j < rows; ++j) {
-                    float a = 0.f, b = 0.f;
-                    for (int q = 0; q < ksplit; ++q) {
-                        const float* r = base + q * sstride + j * (2 * kRowsPerTile);
-                        a += __ldcg(r + row);
-                        b += __ldcg(r + kRowsPerTile + row);
-                    }
-                    if constexpr (W13) {
-                        const int n0 = mt * kRowsPerTile + row;
-                        const int n = p.h_interleaved ? interleave16(n0) : n0;
-                        p.out[static_cast<int64_t>(row0 + j) * p.out_ld + n] = __float2bfloat16_rn(swiglu(a, b, L));
-                    } else {
-                        const int m = mt * 2 * kRowsPerTile + row;
-                        __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + j) * p.out_ld + m;
-                        o[0] = __float2bfloat16_rn(a);
-                        o[kRowsPerTile] = __float2bfloat16_rn(b);
-                    }
-                }
                 continue;
             }
             if constexpr (W13) {
@@ -673,7 +614,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
     const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
-    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2) + 16;
+    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + kMaxIssuers) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);
     if (ns > 8) ns = 8;
@@ -683,7 +624,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     L.off_w = ns * b_stage;
     L.off_s = L.off_w + ns * w_stage;
     L.off_bar = (L.off_s + s_bytes + 7) & ~7;
-    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2) + 16 + 1024;
+    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + kMaxIssuers) + 16 + 1024;
     return L;
 }
 

@@ -32,8 +32,6 @@ struct GemmParams {
     int ksplit;                 // K splits per unit (1: no split)
     float* partial;             // split-K partial sums [ksplit][mt_count][partial_rows][256] fp32
     int partial_rows;           // rows of the permuted token order (R)
-    int* counters;              // split-K arrival counters [units], zero on entry
-    int row_boxes;              // 1: token tiles are loaded one real row at a time
     int h_interleaved;          // w13: store h columns in the interleaved 16-k order (2-bit w2 input)
     int scale_copy_bytes;       // 16, 8 or 4: cp.async size for the scale rows; 0: plain loads
 };
@@ -55,8 +53,7 @@ int set_error(int code, const char* fmt, ...);
 
 // Routing / gather / combine / pack kernels (kernels.cu).
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
-                         int* inv, int4* tiles, int* n_tiles, int* status, int* zero, int n_zero,
-                         cudaStream_t stream);
+                         int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream);
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
                           int K, int interleave, __nv_bfloat16* xp, cudaStream_t stream);
 // dst[i, :] = src[i, :] with every 16-element block in the interleaved K order
@@ -65,6 +62,16 @@ cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64
                                    __nv_bfloat16* dst, cudaStream_t stream);
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
                            __nv_bfloat16* out, cudaStream_t stream);
+// Split-K epilogues (partial sums [ksplit][mt][R][256] fp32, rows < offsets_end):
+//   h[r, n] = bf16(swiglu(sum_s gate, sum_s up)) (column n at its interleaved position if `interleave`)
+cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
+                                int interleave, __nv_bfloat16* h, cudaStream_t stream);
+//   y[r, m] = bf16(sum_s partial)
+cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const int* offsets_end, int K,
+                               __nv_bfloat16* y, cudaStream_t stream);
+//   out[t, m] = bf16( sum_j w[t, j] * bf16(sum_s partial[s][m/256][inv[t, j]][m%256]) )
+cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
+                                    int T, int topk, int K, __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
                         cudaStream_t stream);
 

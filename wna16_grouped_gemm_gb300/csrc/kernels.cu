@@ -66,14 +66,13 @@ __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int& ea, int
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_kernel(const int32_t* __restrict__ ids, int R, int E, int nt, int* __restrict__ counts,
                  int* __restrict__ offsets, int* __restrict__ perm, int* __restrict__ inv, int4* __restrict__ tiles,
-                 int* __restrict__ n_tiles, int* __restrict__ status, int* __restrict__ zero, int n_zero) {
+                 int* __restrict__ n_tiles, int* __restrict__ status) {
     extern __shared__ int sm[];
     int* cnt = sm;                          // [kRouteWarps][E]
     int* scratch = sm + kRouteWarps * E;    // 64 ints
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_trigger();
     if (tid == 0) *status = kStatusOk;
-    for (int i = tid; i < n_zero; i += kRouteThreads) zero[i] = 0;   // split-K arrival counters
 
     const int per_warp = (((R + kRouteWarps - 1) / kRouteWarps) + 31) & ~31;
     const int f0 = warp * per_warp;
@@ -232,6 +231,84 @@ __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restr
     out[static_cast<int64_t>(t) * vec_per_row + v] = o;
 }
 
+__device__ __forceinline__ float swiglu_clamped(float g, float u, float L) {
+    g = fminf(g, L);
+    u = fminf(fmaxf(u, -L), L);
+    return g / (1.0f + expf(-g)) * u;
+}
+
+// Split-K epilogue of w13: one block per valid permuted row, threads over n.
+__global__ void finalize_w13_kernel(const float* __restrict__ partial, int ksplit, int R, const int* __restrict__ offsets_end,
+                                    int N, float L, int interleave, __nv_bfloat16* __restrict__ h) {
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x;
+    if (r >= *offsets_end) return;
+    const int mtc = N / 128;
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+        const int mt = n >> 7, i = n & 127;
+        float g = 0.f, u = 0.f;
+        for (int s = 0; s < ksplit; ++s) {
+            const float* q = partial + ((static_cast<int64_t>(s) * mtc + mt) * R + r) * 256;
+            g += q[i];
+            u += q[128 + i];
+        }
+        int col = n;
+        if (interleave) {
+            const int e = n & 15;
+            col = (n & ~15) | (e < 8 ? 2 * e : 2 * (e - 8) + 1);
+        }
+        h[static_cast<int64_t>(r) * N + col] = __float2bfloat16_rn(swiglu_clamped(g, u, L));
+    }
+}
+
+// Split-K epilogue of w2 (for the stage entry point): y = bf16(sum of splits).
+__global__ void finalize_w2_kernel(const float* __restrict__ partial, int ksplit, int R, const int* __restrict__ offsets_end,
+                                   int K, __nv_bfloat16* __restrict__ y) {
+    pdl_wait();
+    const int r = blockIdx.x;
+    if (r >= *offsets_end) return;
+    const int mtc = K / 256;
+    for (int m = threadIdx.x; m < K; m += blockDim.x) {
+        float a = 0.f;
+        for (int s = 0; s < ksplit; ++s) a += partial[((static_cast<int64_t>(s) * mtc + (m >> 8)) * R + r) * 256 + (m & 255)];
+        y[static_cast<int64_t>(r) * K + m] = __float2bfloat16_rn(a);
+    }
+}
+
+// Combine straight from the w2 split partial sums: y is rounded to BF16 exactly
+// where the unsplit path stores it, then weighted and summed (j ascending).
+__global__ void combine_partials_kernel(const float* __restrict__ partial, int ksplit, int R,
+                                        const float* __restrict__ w, const int* __restrict__ inv, int topk, int K,
+                                        __nv_bfloat16* __restrict__ out) {
+    pdl_wait();
+    const int t = blockIdx.y;
+    const int m0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (m0 >= K) return;
+    const int mtc = K / 256;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = 0; j < topk; ++j) {
+        const int r = inv[t * topk + j];
+        if (r < 0) continue;
+        const float wj = w[t * topk + j];
+        float ysum[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s = 0; s < ksplit; ++s) {
+            const float4 q = *reinterpret_cast<const float4*>(
+                partial + ((static_cast<int64_t>(s) * mtc + (m0 >> 8)) * R + r) * 256 + (m0 & 255));
+            ysum[0] += q.x;
+            ysum[1] += q.y;
+            ysum[2] += q.z;
+            ysum[3] += q.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            acc[i] = __fmaf_rn(wj, __bfloat162float(__float2bfloat16_rn(ysum[i])), acc[i]);
+    }
+    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + static_cast<int64_t>(t) * K + m0);
+    o[0] = __floats2bfloat162_rn(acc[0], acc[1]);
+    o[1] = __floats2bfloat162_rn(acc[2], acc[3]);
+}
+
 // word i <- codes [i*p, (i+1)*p): field j = (code_j + 2^(b-1)) & (2^b - 1) at bits [b*j, b*j+b).
 __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t n_words, int bits, int32_t* __restrict__ packed) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -248,7 +325,7 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t n_words, i
 }  // namespace
 
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm, int* inv,
-                         int4* tiles, int* n_tiles, int* status, int* zero, int n_zero, cudaStream_t stream) {
+                         int4* tiles, int* n_tiles, int* status, cudaStream_t stream) {
     const int smem = (kRouteWarps * E + 64) * static_cast<int>(sizeof(int));
     static bool attr_set = false;
     if (!attr_set) {
@@ -258,7 +335,7 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, 
         attr_set = true;
     }
     route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, nt, counts, offsets, perm, inv, tiles, n_tiles,
-                                                    status, zero, n_zero);
+                                                    status);
     return cudaGetLastError();
 }
 
@@ -289,6 +366,28 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const i
     dim3 grid((vpr + threads - 1) / threads, T);
     return launch_pdl(combine_kernel, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y), weights, inv,
                       topk, vpr, reinterpret_cast<uint4*>(out));
+}
+
+cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
+                                int interleave, __nv_bfloat16* h, cudaStream_t stream) {
+    if (R == 0) return cudaSuccess;
+    return launch_pdl(finalize_w13_kernel, dim3(R), dim3(256), 0, stream, partial, ksplit, R, offsets_end, N, limit,
+                      interleave, h);
+}
+
+cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const int* offsets_end, int K,
+                               __nv_bfloat16* y, cudaStream_t stream) {
+    if (R == 0) return cudaSuccess;
+    return launch_pdl(finalize_w2_kernel, dim3(R), dim3(256), 0, stream, partial, ksplit, R, offsets_end, K, y);
+}
+
+cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
+                                    int T, int topk, int K, __nv_bfloat16* out, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const int threads = 128;
+    dim3 grid((K / 4 + threads - 1) / threads, T);
+    return launch_pdl(combine_partials_kernel, grid, dim3(threads), 0, stream, partial, ksplit, R, weights, inv, topk, K,
+                      out);
 }
 
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
