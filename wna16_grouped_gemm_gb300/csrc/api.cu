@@ -330,11 +330,20 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     // TMEM (512 columns): nacc sets of n_issuers accumulators of nt columns,
     // then A buffers of 128 columns (2 or 3).  A thread can issue a tcgen05.mma
     // only every ~110 cycles, so small token tiles use 4 issuers (row block x
-    // buffer parity) and large ones 2 (one per row block).
-    gp.n_issuers = nt <= 32 ? 4 : 2;
-    gp.nacc = 2 * gp.n_issuers * nt + 2 * 128 <= 512 ? 2 : 1;
-    const int acc_cols = gp.nacc * gp.n_issuers * nt;
-    gp.nabuf = (512 - acc_cols) / 128 < 3 ? (512 - acc_cols) / 128 : 3;
+    // buffer parity) and large ones 2 (one per row block).  2-bit codes with
+    // 16-token tiles take the group-accumulate mode: 6 issuers (row block x
+    // group parity), 4 group slots of 32 columns, 3 A buffers.
+    gp.ga = (bits == 2 && nt == 16 && group % 128 == 0) ? 1 : 0;
+    if (gp.ga) {
+        gp.n_issuers = 6;
+        gp.nacc = 1;
+        gp.nabuf = 3;
+    } else {
+        gp.n_issuers = nt <= 32 ? 4 : 2;
+        gp.nacc = 2 * gp.n_issuers * nt + 2 * 128 <= 512 ? 2 : 1;
+        const int acc_cols = gp.nacc * gp.n_issuers * nt;
+        gp.nabuf = (512 - acc_cols) / 128 < 3 ? (512 - acc_cols) / 128 : 3;
+    }
     gp.off_b = sm.off_b;
     gp.off_w = sm.off_w;
     gp.off_s = sm.off_s;

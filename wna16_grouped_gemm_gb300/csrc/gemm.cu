@@ -45,12 +45,15 @@ constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
 constexpr int kEpilogueWarps = 4;      // 1 per TMEM lane quarter
 constexpr int kIssuerWarp2 = kFirstEpilogueWarp + kEpilogueWarps;
 constexpr int kIssuerWarp3 = kIssuerWarp2 + 1;
-constexpr int kMaxIssuers = 4;
-constexpr int kThreads = 32 * (kIssuerWarp3 + 1);
+constexpr int kIssuerWarp4 = kIssuerWarp3 + 1;
+constexpr int kIssuerWarp5 = kIssuerWarp4 + 1;
+constexpr int kMaxIssuers = 6;
+constexpr int kThreads = 32 * (kIssuerWarp5 + 1);
 constexpr int kRowsPerTile = 128;
 constexpr int kKA = 128;         // K elements per TMEM A buffer (per row block): 64 columns
 constexpr int kMaxABuf = 3;      // TMEM A ring depth (fewer when the accumulators need the columns)
 constexpr int kTmemCols = 512;
+constexpr int kGaSlots = 4;      // group-partial slots (group-accumulate mode), 2 x 16 columns each
 
 struct Ring {
     uint32_t idx = 0, phase = 0;
@@ -71,6 +74,15 @@ struct Ring {
 // 13 + 11 <= 24 bits for the positions used (8, 12, 16), so the single
 // rounding of the FMA has nothing to round.  One cvt.rn.bf16x2 then gives the
 // correctly rounded BF16 weights.
+// (a & b) | c in one LOP3.  Written out because with both b and c constant the
+// compiler otherwise emits two logic instructions (one immediate per LOP3),
+// which nearly doubles the integer-pipe work of the dequantisation.
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
 template <int POS>
 __device__ __forceinline__ uint32_t magic_bits() {
     return static_cast<uint32_t>(150 - POS) << 23;
@@ -79,7 +91,7 @@ __device__ __forceinline__ uint32_t magic_bits() {
 template <int BITS, int POS>
 __device__ __forceinline__ float field_value(uint32_t src, float s, float negoff) {
     constexpr uint32_t mask = ((1u << BITS) - 1u) << POS;
-    const uint32_t b = (src & mask) | magic_bits<POS>();
+    const uint32_t b = and_or(src, mask, magic_bits<POS>());
     return __fmaf_rn(__uint_as_float(b), s, negoff);
 }
 
@@ -129,14 +141,52 @@ struct Scale2 {  // bf16(s) / 4^i as bf16x2, i = 0, 1, 2
 
 __device__ __forceinline__ void dequant_word2_pairs(uint32_t w, const Scale2& c, uint32_t* o) {
     const uint32_t w6 = w >> 6, w12 = w >> 12;
-    o[0] = bf2_mul(bf2_add((w & 0x00030003u) | kBf2Magic, kBf2Neg130), c.s0);    // fields 0, 8
-    o[1] = bf2_mul(bf2_add((w & 0x000C000Cu) | kBf2Magic, kBf2Neg136), c.s1);    // fields 1, 9
-    o[2] = bf2_mul(bf2_add((w & 0x00300030u) | kBf2Magic, kBf2Neg160), c.s2);    // fields 2, 10
-    o[3] = bf2_mul(bf2_add((w6 & 0x00030003u) | kBf2Magic, kBf2Neg130), c.s0);   // fields 3, 11
-    o[4] = bf2_mul(bf2_add((w6 & 0x000C000Cu) | kBf2Magic, kBf2Neg136), c.s1);   // fields 4, 12
-    o[5] = bf2_mul(bf2_add((w6 & 0x00300030u) | kBf2Magic, kBf2Neg160), c.s2);   // fields 5, 13
-    o[6] = bf2_mul(bf2_add((w12 & 0x00030003u) | kBf2Magic, kBf2Neg130), c.s0);  // fields 6, 14
-    o[7] = bf2_mul(bf2_add((w12 & 0x000C000Cu) | kBf2Magic, kBf2Neg136), c.s1);  // fields 7, 15
+    o[0] = bf2_mul(bf2_add(and_or(w, 0x00030003u, kBf2Magic), kBf2Neg130), c.s0);    // fields 0, 8
+    o[1] = bf2_mul(bf2_add(and_or(w, 0x000C000Cu, kBf2Magic), kBf2Neg136), c.s1);    // fields 1, 9
+    o[2] = bf2_mul(bf2_add(and_or(w, 0x00300030u, kBf2Magic), kBf2Neg160), c.s2);    // fields 2, 10
+    o[3] = bf2_mul(bf2_add(and_or(w6, 0x00030003u, kBf2Magic), kBf2Neg130), c.s0);   // fields 3, 11
+    o[4] = bf2_mul(bf2_add(and_or(w6, 0x000C000Cu, kBf2Magic), kBf2Neg136), c.s1);   // fields 4, 12
+    o[5] = bf2_mul(bf2_add(and_or(w6, 0x00300030u, kBf2Magic), kBf2Neg160), c.s2);   // fields 5, 13
+    o[6] = bf2_mul(bf2_add(and_or(w12, 0x00030003u, kBf2Magic), kBf2Neg130), c.s0);  // fields 6, 14
+    o[7] = bf2_mul(bf2_add(and_or(w12, 0x000C000Cu, kBf2Magic), kBf2Neg136), c.s1);  // fields 7, 15
+}
+
+// Group-accumulate mode (2-bit codes, scales applied per group after the MMA):
+// the A operand is the plain code.  A field q OR-ed into mantissa bits 2i..2i+1
+// of 128.0 reads 128 + 4^i q; one bf16x2 FMA by 4^-i with addend
+// -(128 * 4^-i + 2) gives q - 2 = code exactly (the product is exact and the
+// exact sum is a small integer, so the single rounding has nothing to round).
+__device__ __forceinline__ uint32_t bf2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+constexpr uint32_t kBf2One = 0x3F803F80u;       // 1
+constexpr uint32_t kBf2Quarter = 0x3E803E80u;   // 1/4
+constexpr uint32_t kBf2Sixteenth = 0x3D803D80u; // 1/16
+constexpr uint32_t kBf2Neg34 = 0xC208C208u;     // -(32 + 2)
+constexpr uint32_t kBf2Neg10 = 0xC120C120u;     // -(8 + 2)
+
+__device__ __forceinline__ void dequant_word2_codes(uint32_t w, uint32_t* o) {
+    const uint32_t w6 = w >> 6, w12 = w >> 12;
+    o[0] = bf2_fma(and_or(w, 0x00030003u, kBf2Magic), kBf2One, kBf2Neg130);        // fields 0, 8
+    o[1] = bf2_fma(and_or(w, 0x000C000Cu, kBf2Magic), kBf2Quarter, kBf2Neg34);     // fields 1, 9
+    o[2] = bf2_fma(and_or(w, 0x00300030u, kBf2Magic), kBf2Sixteenth, kBf2Neg10);   // fields 2, 10
+    o[3] = bf2_fma(and_or(w6, 0x00030003u, kBf2Magic), kBf2One, kBf2Neg130);       // fields 3, 11
+    o[4] = bf2_fma(and_or(w6, 0x000C000Cu, kBf2Magic), kBf2Quarter, kBf2Neg34);    // fields 4, 12
+    o[5] = bf2_fma(and_or(w6, 0x00300030u, kBf2Magic), kBf2Sixteenth, kBf2Neg10);  // fields 5, 13
+    o[6] = bf2_fma(and_or(w12, 0x00030003u, kBf2Magic), kBf2One, kBf2Neg130);      // fields 6, 14
+    o[7] = bf2_fma(and_or(w12, 0x000C000Cu, kBf2Magic), kBf2Quarter, kBf2Neg34);   // fields 7, 15
+}
+
+// 64 consecutive k of one row -> 32 bf16x2 plain 2-bit codes (same layout as
+// dequant_chunk<2>).
+__device__ __forceinline__ void codes_chunk2(const uint8_t* row, uint32_t xr, int chunk, uint32_t (&o)[32]) {
+    const uint4 v = *reinterpret_cast<const uint4*>(row + ((static_cast<uint32_t>(chunk) ^ xr) << 4));
+    dequant_word2_codes(v.x, o + 0);
+    dequant_word2_codes(v.y, o + 8);
+    dequant_word2_codes(v.z, o + 16);
+    dequant_word2_codes(v.w, o + 24);
 }
 
 // One 4-bit word (8 consecutive k) -> 4 bf16x2.
@@ -228,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nabuf = p.nabuf;
     const int nacc = p.nacc;
     const int n_iss = p.n_issuers;
+    const bool ga = p.ga != 0;     // group-accumulate mode: see the issuer and epilogue sections
 
     uint8_t* sB = smem + p.off_b;
     uint8_t* sW = smem + p.off_w;
@@ -242,7 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* sfull = accempty + 2;
     uint64_t* sempty = sfull + 2;
     uint64_t* drain = sempty + 2;              // [kMaxIssuers]
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
+    uint64_t* gfull = drain + kMaxIssuers;     // [kGaSlots]
+    uint64_t* gempty = gfull + kGaSlots;       // [kGaSlots]
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gempty + kGaSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     if (threadIdx.x == 0) {
@@ -258,9 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&accfull[i], n_iss);
             mbar_init(&accempty[i], kEpilogueWarps);
             mbar_init(&sfull[i], 32);
-            mbar_init(&sempty[i], kDequantWarps);
+            mbar_init(&sempty[i], ga ? kEpilogueWarps : kDequantWarps);   // whoever applies the scales
         }
         for (int i = 0; i < kMaxIssuers; ++i) mbar_init(&drain[i], 1);
+        for (int i = 0; i < kGaSlots; ++i) {
+            mbar_init(&gfull[i], 2);                   // the group's two issuers (row blocks)
+            mbar_init(&gempty[i], kEpilogueWarps);
+        }
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_w);
@@ -285,11 +342,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int kps = ksteps / ksplit;              // stages per item
     const int nbuf_item = kps * chunks;           // TMEM A buffers per item
     int* status = p.status;
-    // TMEM columns: [nacc sets x n_iss accumulators of nt columns] [A buffers of 128 columns]
+    // TMEM columns: [nacc sets x n_iss accumulators of nt columns] [A buffers of 128 columns],
+    // in GA mode [kGaSlots group slots of 2 x 16 columns] [A buffers]
     const uint32_t acc_set_cols = static_cast<uint32_t>(n_iss * nt);
-    const uint32_t abase_col = static_cast<uint32_t>(nacc) * acc_set_cols;
-    const int issuer = warp == kIssuerWarp0 ? 0 : warp == kIssuerWarp1 ? 1 : warp == kIssuerWarp2 ? 2
-                                                                       : warp == kIssuerWarp3 ? 3 : -1;
+    const uint32_t abase_col = ga ? static_cast<uint32_t>(kGaSlots * 2 * 16) : static_cast<uint32_t>(nacc) * acc_set_cols;
+    const int issuer = warp == kIssuerWarp0   ? 0
+                       : warp == kIssuerWarp1 ? 1
+                       : warp == kIssuerWarp2 ? 2
+                       : warp == kIssuerWarp3 ? 3
+                       : warp == kIssuerWarp4 ? 4
+                       : warp == kIssuerWarp5 ? 5
+                                              : -1;
+    // group-accumulate mode: groups of this CTA counted over all its items
+    const int ng_item = p.ngroups / ksplit;       // scale groups per item
+    const int bpg = p.group / kKA;                // A buffers per group (GA mode: group % 128 == 0)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
@@ -340,11 +406,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (issuer >= 0) {
         // ------------------------------------------------------------ MMA issuers
-        // Issuer i owns accumulator i of each set: row block t = i & 1; with 4
-        // issuers, parity h = i >> 1 takes the item's A buffers b with b % 2 == h.
-        // One thread can issue a tcgen05.mma only every ~110 cycles, so several
-        // issuers keep the tensor pipe fed.
-        if (lane == 0 && issuer < n_iss) {
+        // Issuer i serves row block t = i & 1.  One thread can issue a
+        // tcgen05.mma only every ~110 cycles, so several issuers keep the tensor
+        // pipe fed: with 4 issuers, parity h = i >> 1 takes the item's A buffers
+        // b with b % 2 == h, each issuer into its own accumulator (the epilogue
+        // adds them).  In group-accumulate mode (6 issuers) issuer parity
+        // h = i >> 1 takes the groups g with g % 3 == h, and every group is
+        // accumulated from zero into a slot of kGaSlots that the epilogue warps
+        // scale and add up.
+        if (lane == 0 && issuer < n_iss && ga) {
+            const int t = issuer & 1;
+            const int h = issuer >> 1;
+            const int npar = n_iss >> 1;
+            const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
+            Ring st, ab;
+            bool ok = true;
+            bool issued = false;
+            uint32_t gbase = 0;   // groups of the earlier items
+            for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x, gbase += ng_item) {
+                int bl = 0;   // A buffer index within the item
+                for (int ks = 0; ks < kps && ok; ++ks) {
+                    if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bstage = smem_u32(sB + st.idx * b_stage_bytes);
+                    for (int c = 0; c < chunks; ++c, ++bl) {
+                        const uint32_t gc = gbase + static_cast<uint32_t>(bl / bpg);
+                        if (static_cast<int>(gc % npar) == h) {
+                            const uint32_t slot = gc % kGaSlots;
+                            const int bin = bl % bpg;   // buffer within the group
+                            if (bin == 0 && !mbar_wait(&gempty[slot], ((gc / kGaSlots) & 1u) ^ 1u, abort_flag,
+                                                       status)) {
+                                ok = false;
+                                break;
+                            }
+                            if (!mbar_wait(&afull[ab.idx], ab.phase, abort_flag, status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t d = tmem + slot * (2 * 16) + static_cast<uint32_t>(t * 16);
+                            const uint32_t a0 = tmem + abase_col + ab.idx * 128 + t * 64;
+#pragma unroll
+                            for (int k16 = 0; k16 < 8; ++k16) {
+                                const uint32_t batom = bstage + static_cast<uint32_t>((2 * c + (k16 >> 2)) * nt * 128 +
+                                                                                      (k16 & 3) * 32);
+                                tc_mma_ts(d, a0 + k16 * 8, smem_desc_sw128(batom), idesc,
+                                          (bin == 0 && k16 == 0) ? 0u : 1u);
+                            }
+                            issued = true;
+                            tc_commit(&aempty[ab.idx]);
+                            if (bin == bpg - 1) tc_commit(&gfull[slot]);
+                        }
+                        ab.next(nabuf);
+                    }
+                    if (!ok) break;
+                    tc_commit(&empty[st.idx]);
+                    st.next(nstage);
+                }
+            }
+            if (!ok && issued) {
+                tc_commit(&drain[issuer]);
+                const uint32_t a = smem_u32(&drain[issuer]);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(a, 0)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+                }
+            }
+        } else if (lane == 0 && issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
             const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
@@ -406,7 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ scale loader
         Ring sb;
         const int ng = p.ngroups;
-        const int ng_item = ng / ksplit;           // groups of one K split
         const int rb = ng_item * 2;                // scale bytes of one row for one item
         const int cb = p.scale_copy_bytes;         // cp.async size (0: plain loads)
         for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
@@ -456,13 +585,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t abase = tmem + abase_col + lane_base + static_cast<uint32_t>(blk * 64);
         Ring st, ab, sb;
         bool ok = true;
+        int pending = -1;   // A buffer whose stores are issued but not yet waited for
+        const int halves_per_group = p.group / 64;
         for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
             const int u = v / ksplit;
             const int split = v - u * ksplit;
-            const int kbeg = split * kps * kp;
-            if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
-            const int ng_item = p.ngroups / ksplit;
+            // GA mode: the epilogue warps apply the scales, not these warps
+            if (!ga && !mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
             const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + (blk * kRowsPerTile + row) * ng_item;
+            int gi = 0, gleft = halves_per_group;   // scale group of the current 64-k half
             for (int ks = split * kps; ks < (split + 1) * kps && ok; ++ks) {
                 if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
                     ok = false;
@@ -470,26 +601,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* wrow = sW + st.idx * 2 * w_tile_bytes + blk * w_tile_bytes + row * pitch;
                 for (int c = 0; c < chunks; ++c) {
-                    // one TMEM A buffer = 128 k, stored as two 64-k halves (scales
-                    // may differ for group 64); the first store overlaps the second
-                    // half's arithmetic only through the other warps on the scheduler
-                    const int k0 = ks * kp + c * kKA - kbeg;
+                    // one TMEM A buffer = 128 k = two 64-k halves (scales may differ
+                    // for group 64).  A TMEM store takes hundreds of cycles to
+                    // complete, so the wait for a buffer's stores (and its afull
+                    // arrival) is deferred until the first half of the next buffer
+                    // has been dequantised.  Nothing waited on in between depends on
+                    // the pending buffer: its aempty wait comes after the arrival,
+                    // and stage and scale slots are at least double-buffered.
                     uint32_t v32[32];
-                    dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[k0 / p.group])), v32);
+                    if constexpr (BITS == 2) {
+                        if (ga) {
+                            codes_chunk2(wrow, xr, 2 * c, v32);
+                        } else {
+                            dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[gi])), v32);
+                        }
+                    } else {
+                        dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[gi])), v32);
+                    }
+                    if (--gleft == 0) {
+                        gleft = halves_per_group;
+                        ++gi;
+                    }
+                    if (pending >= 0) {
+                        tc_wait_st();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&afull[pending]);
+                        pending = -1;
+                    }
                     if (!mbar_wait(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     tc_st_32x32b_x32(abase + ab.idx * 128, v32);
-                    tc_wait_st();
-                    dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[(k0 + 64) / p.group])),
-                                        v32);
+                    if constexpr (BITS == 2) {
+                        if (ga) {
+                            codes_chunk2(wrow, xr, 2 * c + 1, v32);
+                        } else {
+                            dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[gi])), v32);
+                        }
+                    } else {
+                        dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[gi])), v32);
+                    }
+                    if (--gleft == 0) {
+                        gleft = halves_per_group;
+                        ++gi;
+                    }
                     tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v32);
-                    tc_wait_st();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&afull[ab.idx]);
+                    pending = ab.idx;
                     ab.next(nabuf);
                 }
                 if (!ok) break;
@@ -498,46 +658,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 st.next(nstage);
             }
             if (!ok) break;
+            if (!ga) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[sb.idx]);
+                sb.next(2);
+            }
+        }
+        if (pending >= 0) {   // also drains the stores on the abort path
+            tc_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sempty[sb.idx]);
-            sb.next(2);
+            if (lane == 0) mbar_arrive(&afull[pending]);
         }
     } else if (warp >= kFirstEpilogueWarp && warp < kFirstEpilogueWarp + kEpilogueWarps) {
         // ------------------------------------------------------------ epilogue
-        // thread = TMEM lane = weight row `row` of both row blocks; a row
-        // block's sum is its issuers' accumulators added (one or two parities)
+        // thread = TMEM lane = weight row `row` of both row blocks
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const float L = p.limit;
-        const int nh = (n_iss == 4 && nbuf_item >= 2) ? 2 : 1;
-        Ring acc;
-        for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
-            const int u = v / ksplit;
-            const int split = v - u * ksplit;
-            const int4 tile = p.tiles[u / p.mt_count];
-            const int mt = u % p.mt_count;
-            const int rows = tile.z;
-            const int row0 = tile.y;
-            if (!mbar_wait_bounded(&accfull[acc.idx], acc.phase, abort_flag, status, true)) break;
-            tc_fence_after();
-            const uint32_t a0 = tmem + lane_base + acc.idx * acc_set_cols;   // issuer i at + i * nt
-            // sums of both row blocks for token columns j0..j0+7
-            auto load8 = [&](int j0, float (&s0)[8], float (&s1)[8]) {
-                uint32_t d[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) s0[i] = s1[i] = 0.f;
-                for (int hh = 0; hh < nh; ++hh) {
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>((2 * hh) * nt + j0), d);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) s0[i] += __uint_as_float(d[i]);
-                    tc_ld_32x32b_x8(a0 + static_cast<uint32_t>((2 * hh + 1) * nt + j0), d);
-                    tc_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) s1[i] += __uint_as_float(d[i]);
-                }
-            };
+        // Writes one item's result for its token columns 0..rows-1;
+        // load16(j0, s0, s1) yields both row blocks' sums for columns j0..j0+15.
+        auto emit = [&](int split, int mt, int rows, int row0, auto&& load16) {
             if (ksplit > 1) {
                 // Split K: park this split's fp32 sums for the tile's real token
                 // rows in partial[split][mt][permuted row][256 weight rows]; a
@@ -546,43 +688,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t R_rows = p.partial_rows;
                 float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
                                               (2 * kRowsPerTile) + row;
-                for (int j0 = 0; j0 < rows; j0 += 8) {
-                    float s0[8], s1[8];
-                    load8(j0, s0, s1);
+                for (int j0 = 0; j0 < rows; j0 += 16) {
+                    float s0[16], s1[16];
+                    load16(j0, s0, s1);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         if (j0 + i < rows) {
                             mine[(j0 + i) * (2 * kRowsPerTile)] = s0[i];
                             mine[(j0 + i) * (2 * kRowsPerTile) + kRowsPerTile] = s1[i];
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&accempty[acc.idx]);
-                acc.next(nacc);
-                continue;
+                return;
             }
             if constexpr (W13) {
                 // gate = block 0, up = block 1 of the same lane
                 const int n0 = mt * kRowsPerTile + row;
                 const int n = p.h_interleaved ? interleave16(n0) : n0;
-                for (int j0 = 0; j0 < rows; j0 += 8) {
-                    float g[8], uu[8];
-                    load8(j0, g, uu);
+                for (int j0 = 0; j0 < rows; j0 += 16) {
+                    float g[16], uu[16];
+                    load16(j0, g, uu);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
+                    for (int i = 0; i < 16; ++i)
                         if (j0 + i < rows)
                             p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + n] =
                                 __float2bfloat16_rn(swiglu(g[i], uu[i], L));
                 }
             } else {
                 const int m = mt * 2 * kRowsPerTile + row;
-                for (int j0 = 0; j0 < rows; j0 += 8) {
-                    float y0[8], y1[8];
-                    load8(j0, y0, y1);
+                for (int j0 = 0; j0 < rows; j0 += 16) {
+                    float y0[16], y1[16];
+                    load16(j0, y0, y1);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
+                    for (int i = 0; i < 16; ++i) {
                         if (j0 + i < rows) {
                             __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + j0 + i) * p.out_ld + m;
                             o[0] = __float2bfloat16_rn(y0[i]);
@@ -591,10 +729,107 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[acc.idx]);
-            acc.next(nacc);
+        };
+        if (ga) {
+            // Group-accumulate mode (2-bit codes, 16-token tiles): every group's
+            // code sums arrive in a TMEM slot; this row's sums add
+            // bf16(scale) * slot in group order.  For 2-bit codes (0 or +-2^j)
+            // code * bf16(scale) is exactly the BF16-rounded dequantised weight,
+            // so this is the same sum as with dequantised weights.
+            Ring sb;
+            uint32_t gbase = 0;
+            bool ok = true;
+            for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x, gbase += ng_item) {
+                const int u = v / ksplit;
+                const int split = v - u * ksplit;
+                const int4 tile = p.tiles[u / p.mt_count];
+                if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
+                const uint16_t* s0row = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + row * ng_item;
+                const uint16_t* s1row = s0row + kRowsPerTile * ng_item;
+                float y0[16], y1[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) y0[i] = y1[i] = 0.0f;
+                for (int g = 0; g < ng_item; ++g) {
+                    const uint32_t gc = gbase + static_cast<uint32_t>(g);
+                    const uint32_t slot = gc % kGaSlots;
+                    if (!mbar_wait(&gfull[slot], (gc / kGaSlots) & 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t d0[16], d1[16];
+                    tc_ld_32x32b_x16(tmem + lane_base + slot * (2 * 16), d0);
+                    tc_ld_32x32b_x16(tmem + lane_base + slot * (2 * 16) + 16, d1);
+                    tc_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&gempty[slot]);
+                    const float c0 = __bfloat162float(__float2bfloat16_rn(__half2float(__ushort_as_half(s0row[g]))));
+                    const float c1 = __bfloat162float(__float2bfloat16_rn(__half2float(__ushort_as_half(s1row[g]))));
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        y0[i] = __fmaf_rn(c0, __uint_as_float(d0[i]), y0[i]);
+                        y1[i] = __fmaf_rn(c1, __uint_as_float(d1[i]), y1[i]);
+                    }
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sempty[sb.idx]);
+                sb.next(2);
+                emit(split, u % p.mt_count, tile.z, tile.y, [&](int, float (&s0)[16], float (&s1)[16]) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        s0[i] = y0[i];
+                        s1[i] = y1[i];
+                    }
+                });
+            }
+        } else {
+            // a row block's sum is its issuers' accumulators added (one or two parities)
+            const int nh = (n_iss == 4 && nbuf_item >= 2) ? 2 : 1;
+            Ring acc;
+            for (int v = blockIdx.x; v < n_items; v += gridDim.x) {
+                const int u = v / ksplit;
+                const int split = v - u * ksplit;
+                const int4 tile = p.tiles[u / p.mt_count];
+                if (!mbar_wait_bounded(&accfull[acc.idx], acc.phase, abort_flag, status, true)) break;
+                tc_fence_after();
+                const uint32_t a0 = tmem + lane_base + acc.idx * acc_set_cols;   // issuer i at + i * nt
+                // every load of a 16-column group is issued before the one wait
+                // (TMEM loads take hundreds of cycles to complete)
+                emit(split, u % p.mt_count, tile.z, tile.y, [&](int j0, float (&s0)[16], float (&s1)[16]) {
+                    if (nh == 1) {
+                        uint32_t d0[16], d1[16];
+                        tc_ld_32x32b_x16(a0 + static_cast<uint32_t>(j0), d0);
+                        tc_ld_32x32b_x16(a0 + static_cast<uint32_t>(nt + j0), d1);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            s0[i] = __uint_as_float(d0[i]);
+                            s1[i] = __uint_as_float(d1[i]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; q += 8) {
+                            uint32_t d0[8], d1[8], d2[8], d3[8];
+                            tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0 + q), d0);
+                            tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0 + q), d1);
+                            tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(2 * nt + j0 + q), d2);
+                            tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(3 * nt + j0 + q), d3);
+                            tc_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                s0[q + i] = __uint_as_float(d0[i]) + __uint_as_float(d2[i]);
+                                s1[q + i] = __uint_as_float(d1[i]) + __uint_as_float(d3[i]);
+                            }
+                        }
+                    }
+                });
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[acc.idx]);
+                acc.next(nacc);
+            }
         }
     }
 
@@ -614,7 +849,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
     const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
-    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + kMaxIssuers) + 16;
+    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2 * kGaSlots) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);
     if (ns > 8) ns = 8;
@@ -624,7 +859,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     L.off_w = ns * b_stage;
     L.off_s = L.off_w + ns * w_stage;
     L.off_bar = (L.off_s + s_bytes + 7) & ~7;
-    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + kMaxIssuers) + 16 + 1024;
+    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2 * kGaSlots) + 16 + 1024;
     return L;
 }
 
