@@ -332,12 +332,14 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     // only every ~110 cycles, so small token tiles use 4 issuers (row block x
     // buffer parity) and large ones 2 (one per row block).  2-bit codes with
     // 16-token tiles take the group-accumulate mode: 6 issuers (row block x
-    // group parity), 4 group slots of 32 columns, 3 A buffers.
-    gp.ga = (bits == 2 && nt == 16 && group % 128 == 0) ? 1 : 0;
+    // group parity), 3 group slots of 32 columns, 3 A buffers.
+    gp.dequant_warps = 8;
+    // group-accumulate mode: one A buffer per scale group (group == 128 k)
+    gp.ga = (bits == 2 && nt == 16 && group == 128) ? 1 : 0;
     if (gp.ga) {
         gp.n_issuers = 6;
         gp.nacc = 1;
-        gp.nabuf = 3;
+        gp.nabuf = 3;   // A buffers (128 columns each) after the 128 columns of group slots
     } else {
         gp.n_issuers = nt <= 32 ? 4 : 2;
         gp.nacc = 2 * gp.n_issuers * nt + 2 * 128 <= 512 ? 2 : 1;

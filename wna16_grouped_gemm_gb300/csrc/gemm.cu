@@ -33,27 +33,40 @@ namespace wna16 {
 
 namespace {
 
-// Warp roles (18 warps).
+// Warp roles: producer, scale loader, issuers 0-1, DW = 8 dequant warps (one
+// per 128-row block and TMEM lane quarter), 4 epilogue warps (one per lane
+// quarter), issuers 2-5.  A warp can only reach the TMEM lanes of its quarter
+// (warp index % 4), which the dequant and epilogue ranges, starting at
+// multiples of 4, respect.
 constexpr int kProducerWarp = 0;       // TMA
 constexpr int kScaleWarp = 1;          // cp.async of the scales
 constexpr int kIssuerWarp0 = 2;        // MMA issuers; warp 2 also owns the TMEM allocation
 constexpr int kIssuerWarp1 = 3;
 constexpr int kAllocWarp = kIssuerWarp0;
 constexpr int kFirstDequantWarp = 4;
-constexpr int kDequantWarps = 8;       // 2 per TMEM lane quarter: one per 128-row block
-constexpr int kFirstEpilogueWarp = kFirstDequantWarp + kDequantWarps;
-constexpr int kEpilogueWarps = 4;      // 1 per TMEM lane quarter
-constexpr int kIssuerWarp2 = kFirstEpilogueWarp + kEpilogueWarps;
-constexpr int kIssuerWarp3 = kIssuerWarp2 + 1;
-constexpr int kIssuerWarp4 = kIssuerWarp3 + 1;
-constexpr int kIssuerWarp5 = kIssuerWarp4 + 1;
+constexpr int kEpilogueWarps = 4;
 constexpr int kMaxIssuers = 6;
-constexpr int kThreads = 32 * (kIssuerWarp5 + 1);
+template <int DW>
+struct Roles {
+    static constexpr int kFirstEpilogueWarp = kFirstDequantWarp + DW;
+    static constexpr int kIssuerWarp2 = kFirstEpilogueWarp + kEpilogueWarps;
+    static constexpr int kThreads = 32 * (kIssuerWarp2 + 4);
+};
 constexpr int kRowsPerTile = 128;
 constexpr int kKA = 128;         // K elements per TMEM A buffer (per row block): 64 columns
 constexpr int kMaxABuf = 3;      // TMEM A ring depth (fewer when the accumulators need the columns)
 constexpr int kTmemCols = 512;
-constexpr int kGaSlots = 4;      // group-partial slots (group-accumulate mode), 2 x 16 columns each
+// Group-partial slots of the group-accumulate mode (2 x 16 columns each): one
+// per issuer parity, so that a slot is always refilled by the issuer that
+// filled it before.  An mbarrier parity wait is only sound when the barrier
+// can be neither two phases behind the waiter (the wait would pass early) nor
+// two phases ahead (it would wait for a later phase).  Every wait here is on
+// a barrier whose phases the waiter's own earlier waits and arrivals order:
+// the dequant warps and the epilogue wait on every phase of theirs; an issuer
+// waits on the A buffers and group slots of its own parity only, which with
+// 3 A buffers and 3 parities (GA) or in-order afull completions (4 issuers)
+// keeps it within one phase.
+constexpr int kGaSlots = 3;
 
 struct Ring {
     uint32_t idx = 0, phase = 0;
@@ -257,11 +270,15 @@ __device__ __forceinline__ void unit_rows(const GemmParams& p, int e, int mt, in
 
 }  // namespace
 
-template <int BITS, bool W13>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BITS, bool W13, int DW, bool GA>
+__global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                         const GemmParams p) {
     constexpr int kCodes = 32 / BITS;
+    constexpr int kDequantWarps = DW;
+    constexpr int kFirstEpilogueWarp = Roles<DW>::kFirstEpilogueWarp;
+    constexpr int kIssuerWarp2 = Roles<DW>::kIssuerWarp2;
+    constexpr int kEW = DW == 16 ? 8 : 16;   // epilogue column chunk (fits the register budget)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
 
@@ -278,7 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nabuf = p.nabuf;
     const int nacc = p.nacc;
     const int n_iss = p.n_issuers;
-    const bool ga = p.ga != 0;     // group-accumulate mode: see the issuer and epilogue sections
+    static_assert(!GA || BITS == 2, "group-accumulate mode: 2-bit codes");
+    static_assert(DW == 8, "8 dequant warps: one per row block and TMEM lane quarter");
+    constexpr bool ga = GA;   // group-accumulate mode: see the issuer and epilogue sections
 
     uint8_t* sB = smem + p.off_b;
     uint8_t* sW = smem + p.off_w;
@@ -304,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&empty[i], kDequantWarps + n_iss);
         }
         for (int i = 0; i < kMaxABuf; ++i) {
-            mbar_init(&afull[i], kDequantWarps);
+            mbar_init(&afull[i], 8);                // the 8 dequant warps that fill it
             mbar_init(&aempty[i], 2);              // the two issuers (row blocks) that read it
         }
         for (int i = 0; i < 2; ++i) {
@@ -343,19 +362,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nbuf_item = kps * chunks;           // TMEM A buffers per item
     int* status = p.status;
     // TMEM columns: [nacc sets x n_iss accumulators of nt columns] [A buffers of 128 columns],
-    // in GA mode [kGaSlots group slots of 2 x 16 columns] [A buffers]
+    // in GA mode [kGaSlots group slots of 2 x 16 columns, padded to 128] [A buffers]
     const uint32_t acc_set_cols = static_cast<uint32_t>(n_iss * nt);
-    const uint32_t abase_col = ga ? static_cast<uint32_t>(kGaSlots * 2 * 16) : static_cast<uint32_t>(nacc) * acc_set_cols;
-    const int issuer = warp == kIssuerWarp0   ? 0
-                       : warp == kIssuerWarp1 ? 1
-                       : warp == kIssuerWarp2 ? 2
-                       : warp == kIssuerWarp3 ? 3
-                       : warp == kIssuerWarp4 ? 4
-                       : warp == kIssuerWarp5 ? 5
-                                              : -1;
+    const uint32_t abase_col = ga ? 128u : static_cast<uint32_t>(nacc) * acc_set_cols;
+    const int issuer = warp == kIssuerWarp0                                ? 0
+                       : warp == kIssuerWarp1                             ? 1
+                       : (warp >= kIssuerWarp2 && warp < kIssuerWarp2 + 4) ? 2 + (warp - kIssuerWarp2)
+                                                                           : -1;
     // group-accumulate mode: groups of this CTA counted over all its items
     const int ng_item = p.ngroups / ksplit;       // scale groups per item
-    const int bpg = p.group / kKA;                // A buffers per group (GA mode: group % 128 == 0)
+    const int bpg = p.group / kKA;                // A buffers per scale group
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
@@ -414,7 +430,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // h = i >> 1 takes the groups g with g % 3 == h, and every group is
         // accumulated from zero into a slot of kGaSlots that the epilogue warps
         // scale and add up.
-        if (lane == 0 && issuer < n_iss && ga) {
+        if constexpr (GA) {
+          if (lane == 0 && issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
             const int npar = n_iss >> 1;
@@ -450,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const uint32_t a0 = tmem + abase_col + ab.idx * 128 + t * 64;
 #pragma unroll
                             for (int k16 = 0; k16 < 8; ++k16) {
+                                // B: 64-k swizzle atom (2c + k16/4), 32 B per 16 k inside it
                                 const uint32_t batom = bstage + static_cast<uint32_t>((2 * c + (k16 >> 2)) * nt * 128 +
                                                                                       (k16 & 3) * 32);
                                 tc_mma_ts(d, a0 + k16 * 8, smem_desc_sw128(batom), idesc,
@@ -474,6 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (globaltimer_ns() - t0 > kWaitLimitNs) break;
                 }
             }
+          }
         } else if (lane == 0 && issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
@@ -594,6 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ga && !mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
             const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + (blk * kRowsPerTile + row) * ng_item;
             int gi = 0, gleft = halves_per_group;   // scale group of the current 64-k half
+            auto next_half = [&]() {
+                if (--gleft == 0) {
+                    gleft = halves_per_group;
+                    ++gi;
+                }
+            };
             for (int ks = split * kps; ks < (split + 1) * kps && ok; ++ks) {
                 if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
                     ok = false;
@@ -607,7 +632,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // arrival) is deferred until the first half of the next buffer
                     // has been dequantised.  Nothing waited on in between depends on
                     // the pending buffer: its aempty wait comes after the arrival,
-                    // and stage and scale slots are at least double-buffered.
+                    // and stage and scale slots are double-buffered.  Every warp
+                    // arrives on the buffers in order, so afull phases complete in
+                    // order, which the issuers' parity waits rely on.
                     uint32_t v32[32];
                     if constexpr (BITS == 2) {
                         if (ga) {
@@ -618,10 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[gi])), v32);
                     }
-                    if (--gleft == 0) {
-                        gleft = halves_per_group;
-                        ++gi;
-                    }
+                    next_half();
                     if (pending >= 0) {
                         tc_wait_st();
                         tc_fence_before();
@@ -644,10 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[gi])), v32);
                     }
-                    if (--gleft == 0) {
-                        gleft = halves_per_group;
-                        ++gi;
-                    }
+                    next_half();
                     tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v32);
                     pending = ab.idx;
                     ab.next(nabuf);
@@ -678,8 +699,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const float L = p.limit;
         // Writes one item's result for its token columns 0..rows-1;
-        // load16(j0, s0, s1) yields both row blocks' sums for columns j0..j0+15.
-        auto emit = [&](int split, int mt, int rows, int row0, auto&& load16) {
+        // load(j0, s0, s1) yields both row blocks' sums for columns j0..j0+kEW-1.
+        auto emit = [&](int split, int mt, int rows, int row0, auto&& load) {
             if (ksplit > 1) {
                 // Split K: park this split's fp32 sums for the tile's real token
                 // rows in partial[split][mt][permuted row][256 weight rows]; a
@@ -688,11 +709,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t R_rows = p.partial_rows;
                 float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
                                               (2 * kRowsPerTile) + row;
-                for (int j0 = 0; j0 < rows; j0 += 16) {
-                    float s0[16], s1[16];
-                    load16(j0, s0, s1);
+                for (int j0 = 0; j0 < rows; j0 += kEW) {
+                    float s0[kEW], s1[kEW];
+                    load(j0, s0, s1);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < kEW; ++i) {
                         if (j0 + i < rows) {
                             mine[(j0 + i) * (2 * kRowsPerTile)] = s0[i];
                             mine[(j0 + i) * (2 * kRowsPerTile) + kRowsPerTile] = s1[i];
@@ -705,22 +726,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // gate = block 0, up = block 1 of the same lane
                 const int n0 = mt * kRowsPerTile + row;
                 const int n = p.h_interleaved ? interleave16(n0) : n0;
-                for (int j0 = 0; j0 < rows; j0 += 16) {
-                    float g[16], uu[16];
-                    load16(j0, g, uu);
+                for (int j0 = 0; j0 < rows; j0 += kEW) {
+                    float g[kEW], uu[kEW];
+                    load(j0, g, uu);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
+                    for (int i = 0; i < kEW; ++i)
                         if (j0 + i < rows)
                             p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + n] =
                                 __float2bfloat16_rn(swiglu(g[i], uu[i], L));
                 }
             } else {
                 const int m = mt * 2 * kRowsPerTile + row;
-                for (int j0 = 0; j0 < rows; j0 += 16) {
-                    float y0[16], y1[16];
-                    load16(j0, y0, y1);
+                for (int j0 = 0; j0 < rows; j0 += kEW) {
+                    float y0[kEW], y1[kEW];
+                    load(j0, y0, y1);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < kEW; ++i) {
                         if (j0 + i < rows) {
                             __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + j0 + i) * p.out_ld + m;
                             o[0] = __float2bfloat16_rn(y0[i]);
@@ -730,59 +751,147 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         };
-        if (ga) {
-            // Group-accumulate mode (2-bit codes, 16-token tiles): every group's
-            // code sums arrive in a TMEM slot; this row's sums add
-            // bf16(scale) * slot in group order.  For 2-bit codes (0 or +-2^j)
-            // code * bf16(scale) is exactly the BF16-rounded dequantised weight,
-            // so this is the same sum as with dequantised weights.
-            Ring sb;
-            uint32_t gbase = 0;
-            bool ok = true;
-            for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x, gbase += ng_item) {
-                const int u = v / ksplit;
-                const int split = v - u * ksplit;
-                const int4 tile = p.tiles[u / p.mt_count];
-                if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
-                const uint16_t* s0row = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + row * ng_item;
-                const uint16_t* s1row = s0row + kRowsPerTile * ng_item;
-                float y0[16], y1[16];
+        // Same, from sums held in registers (columns 0..N-1).
+        auto emit_regs = [&](int split, int mt, int rows, int row0, const auto& y0, const auto& y1) {
+            constexpr int N = sizeof(y0) / sizeof(y0[0]);
+            if (ksplit > 1) {
+                const int64_t R_rows = p.partial_rows;
+                float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
+                                              (2 * kRowsPerTile) + row;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) y0[i] = y1[i] = 0.0f;
-                for (int g = 0; g < ng_item; ++g) {
-                    const uint32_t gc = gbase + static_cast<uint32_t>(g);
-                    const uint32_t slot = gc % kGaSlots;
-                    if (!mbar_wait(&gfull[slot], (gc / kGaSlots) & 1u, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    uint32_t d0[16], d1[16];
-                    tc_ld_32x32b_x16(tmem + lane_base + slot * (2 * 16), d0);
-                    tc_ld_32x32b_x16(tmem + lane_base + slot * (2 * 16) + 16, d1);
-                    tc_wait_ld();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&gempty[slot]);
-                    const float c0 = __bfloat162float(__float2bfloat16_rn(__half2float(__ushort_as_half(s0row[g]))));
-                    const float c1 = __bfloat162float(__float2bfloat16_rn(__half2float(__ushort_as_half(s1row[g]))));
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        y0[i] = __fmaf_rn(c0, __uint_as_float(d0[i]), y0[i]);
-                        y1[i] = __fmaf_rn(c1, __uint_as_float(d1[i]), y1[i]);
+                for (int i = 0; i < N; ++i) {
+                    if (i < rows) {
+                        mine[i * (2 * kRowsPerTile)] = y0[i];
+                        mine[i * (2 * kRowsPerTile) + kRowsPerTile] = y1[i];
                     }
                 }
-                if (!ok) break;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sempty[sb.idx]);
-                sb.next(2);
-                emit(split, u % p.mt_count, tile.z, tile.y, [&](int, float (&s0)[16], float (&s1)[16]) {
+                return;
+            }
+            if constexpr (W13) {
+                const int n0 = mt * kRowsPerTile + row;
+                const int n = p.h_interleaved ? interleave16(n0) : n0;
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        s0[i] = y0[i];
-                        s1[i] = y1[i];
+                for (int i = 0; i < N; ++i)
+                    if (i < rows)
+                        p.out[static_cast<int64_t>(row0 + i) * p.out_ld + n] = __float2bfloat16_rn(swiglu(y0[i], y1[i], L));
+            } else {
+                const int m = mt * 2 * kRowsPerTile + row;
+#pragma unroll
+                for (int i = 0; i < N; ++i) {
+                    if (i < rows) {
+                        __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + i) * p.out_ld + m;
+                        o[0] = __float2bfloat16_rn(y0[i]);
+                        o[kRowsPerTile] = __float2bfloat16_rn(y1[i]);
                     }
-                });
+                }
+            }
+        };
+        if constexpr (GA) {
+            {
+                // Group-accumulate mode (2-bit codes, 16-token tiles): every group's
+                // code sums arrive in a TMEM slot; this row's sums add
+                // bf16(scale) * slot in group order.  For 2-bit codes (0 or +-2^j)
+                // code * bf16(scale) is exactly the BF16-rounded dequantised
+                // weight, so this is the same sum as with dequantised weights.
+                // Tiles of at most 8 tokens (decode) read 8 columns per block and
+                // take two groups per TMEM load wait.
+                Ring sb;
+                uint32_t gbase = 0;
+                bool ok = true;
+                auto scale_of = [](uint16_t h) {
+                    return __bfloat162float(__float2bfloat16_rn(__half2float(__ushort_as_half(h))));
+                };
+                for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x, gbase += ng_item) {
+                    const int u = v / ksplit;
+                    const int split = v - u * ksplit;
+                    const int4 tile = p.tiles[u / p.mt_count];
+                    if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
+                    const uint16_t* s0row = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + row * ng_item;
+                    const uint16_t* s1row = s0row + kRowsPerTile * ng_item;
+                    if (tile.z <= 8) {
+                        float y0[8], y1[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) y0[i] = y1[i] = 0.0f;
+                        for (int g = 0; g < ng_item && ok; g += 2) {
+                            const int n2 = g + 1 < ng_item ? 2 : 1;
+                            for (int j = 0; j < n2; ++j) {
+                                const uint32_t gc = gbase + static_cast<uint32_t>(g + j);
+                                if (!mbar_wait(&gfull[gc % kGaSlots], (gc / kGaSlots) & 1u, abort_flag, status)) {
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                            if (!ok) break;
+                            tc_fence_after();
+                            uint32_t d[2][2][8];
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                if (j < n2) {
+                                    const uint32_t col = ((gbase + static_cast<uint32_t>(g + j)) % kGaSlots) * (2 * 16);
+                                    tc_ld_32x32b_x8(tmem + lane_base + col, d[j][0]);
+                                    tc_ld_32x32b_x8(tmem + lane_base + col + 16, d[j][1]);
+                                }
+                            }
+                            tc_wait_ld();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0)
+                                for (int j = 0; j < n2; ++j) mbar_arrive(&gempty[(gbase + g + j) % kGaSlots]);
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                if (j < n2) {
+                                    const float c0 = scale_of(s0row[g + j]);
+                                    const float c1 = scale_of(s1row[g + j]);
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) {
+                                        y0[i] = __fmaf_rn(c0, __uint_as_float(d[j][0][i]), y0[i]);
+                                        y1[i] = __fmaf_rn(c1, __uint_as_float(d[j][1][i]), y1[i]);
+                                    }
+                                }
+                            }
+                        }
+                        if (!ok) break;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sempty[sb.idx]);
+                        sb.next(2);
+                        emit_regs(split, u % p.mt_count, tile.z, tile.y, y0, y1);
+                    } else {
+                        float y0[16], y1[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) y0[i] = y1[i] = 0.0f;
+                        for (int g = 0; g < ng_item; ++g) {
+                            const uint32_t gc = gbase + static_cast<uint32_t>(g);
+                            const uint32_t col = (gc % kGaSlots) * (2 * 16);
+                            if (!mbar_wait(&gfull[gc % kGaSlots], (gc / kGaSlots) & 1u, abort_flag, status)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const float c0 = scale_of(s0row[g]);
+                            const float c1 = scale_of(s1row[g]);
+#pragma unroll
+                            for (int q = 0; q < 16; q += 8) {
+                                uint32_t d0[8], d1[8];
+                                tc_ld_32x32b_x8(tmem + lane_base + col + q, d0);
+                                tc_ld_32x32b_x8(tmem + lane_base + col + 16 + q, d1);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 8; ++i) {
+                                    y0[q + i] = __fmaf_rn(c0, __uint_as_float(d0[i]), y0[q + i]);
+                                    y1[q + i] = __fmaf_rn(c1, __uint_as_float(d1[i]), y1[q + i]);
+                                }
+                            }
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&gempty[gc % kGaSlots]);
+                        }
+                        if (!ok) break;
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sempty[sb.idx]);
+                        sb.next(2);
+                        emit_regs(split, u % p.mt_count, tile.z, tile.y, y0, y1);
+                    }
+                }
             }
         } else {
             // a row block's sum is its issuers' accumulators added (one or two parities)
@@ -795,22 +904,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait_bounded(&accfull[acc.idx], acc.phase, abort_flag, status, true)) break;
                 tc_fence_after();
                 const uint32_t a0 = tmem + lane_base + acc.idx * acc_set_cols;   // issuer i at + i * nt
-                // every load of a 16-column group is issued before the one wait
+                // every load of a column chunk is issued before the one wait
                 // (TMEM loads take hundreds of cycles to complete)
-                emit(split, u % p.mt_count, tile.z, tile.y, [&](int j0, float (&s0)[16], float (&s1)[16]) {
+                emit(split, u % p.mt_count, tile.z, tile.y, [&](int j0, float (&s0)[kEW], float (&s1)[kEW]) {
                     if (nh == 1) {
-                        uint32_t d0[16], d1[16];
-                        tc_ld_32x32b_x16(a0 + static_cast<uint32_t>(j0), d0);
-                        tc_ld_32x32b_x16(a0 + static_cast<uint32_t>(nt + j0), d1);
+                        uint32_t d0[kEW], d1[kEW];
+                        if constexpr (kEW == 16) {
+                            tc_ld_32x32b_x16(a0 + static_cast<uint32_t>(j0), d0);
+                            tc_ld_32x32b_x16(a0 + static_cast<uint32_t>(nt + j0), d1);
+                        } else {
+                            tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0), d0);
+                            tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0), d1);
+                        }
                         tc_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
+                        for (int i = 0; i < kEW; ++i) {
                             s0[i] = __uint_as_float(d0[i]);
                             s1[i] = __uint_as_float(d1[i]);
                         }
                     } else {
 #pragma unroll
-                        for (int q = 0; q < 16; q += 8) {
+                        for (int q = 0; q < kEW; q += 8) {
                             uint32_t d0[8], d1[8], d2[8], d3[8];
                             tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(j0 + q), d0);
                             tc_ld_32x32b_x8(a0 + static_cast<uint32_t>(nt + j0 + q), d1);
@@ -863,26 +977,37 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     return L;
 }
 
-template <int BITS, bool W13>
+template <int BITS, bool W13, int DW, bool GA>
 static cudaError_t launch_impl(const CUtensorMap& tm_w, const CUtensorMap& tm_b, const GemmParams& p, int grid,
                                int smem_bytes, cudaStream_t stream) {
-    auto kern = grouped_gemm_kernel<BITS, W13>;
+    auto kern = grouped_gemm_kernel<BITS, W13, DW, GA>;
     static int attr_bytes = 0;   // largest dynamic smem size already allowed for this kernel
     if (smem_bytes > attr_bytes) {
         cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (err != cudaSuccess) return err;
         attr_bytes = smem_bytes;
     }
-    return launch_pdl(kern, dim3(grid), dim3(kThreads), static_cast<size_t>(smem_bytes), stream, tm_w, tm_b, p);
+    return launch_pdl(kern, dim3(grid), dim3(Roles<DW>::kThreads), static_cast<size_t>(smem_bytes), stream, tm_w,
+                      tm_b, p);
+}
+
+template <int BITS, bool W13>
+static cudaError_t launch_dw(const CUtensorMap& tm_w, const CUtensorMap& tm_b, const GemmParams& p, int grid,
+                             int smem_bytes, cudaStream_t stream) {
+    if (p.dequant_warps != 8) return cudaErrorInvalidValue;
+    if constexpr (BITS == 2) {
+        if (p.ga) return launch_impl<BITS, W13, 8, true>(tm_w, tm_b, p, grid, smem_bytes, stream);
+    }
+    return launch_impl<BITS, W13, 8, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
 }
 
 cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, const CUtensorMap& tm_b,
                                 const GemmParams& p, int grid, int smem_bytes, cudaStream_t stream) {
     if (bits == 2)
-        return w13 ? launch_impl<2, true>(tm_w, tm_b, p, grid, smem_bytes, stream)
-                   : launch_impl<2, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
-    return w13 ? launch_impl<4, true>(tm_w, tm_b, p, grid, smem_bytes, stream)
-               : launch_impl<4, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
+        return w13 ? launch_dw<2, true>(tm_w, tm_b, p, grid, smem_bytes, stream)
+                   : launch_dw<2, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
+    return w13 ? launch_dw<4, true>(tm_w, tm_b, p, grid, smem_bytes, stream)
+               : launch_dw<4, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
 }
 
 }  // namespace wna16
