@@ -306,8 +306,8 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     uint64_t* full = bars;
     uint64_t* empty = full + nstage;
     uint64_t* afull = empty + nstage;
-    uint64_t* aempty = afull + kMaxABuf;
-    uint64_t* accfull = aempty + kMaxABuf;     // [2]
+    uint64_t* aempty = afull + 2 * kMaxABuf;   // afull/aempty: [A buffer][row block]
+    uint64_t* accfull = aempty + 2 * kMaxABuf; // [2]
     uint64_t* accempty = accfull + 2;          // [2]
     uint64_t* sfull = accempty + 2;
     uint64_t* sempty = sfull + 2;
@@ -322,9 +322,9 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kDequantWarps + n_iss);
         }
-        for (int i = 0; i < kMaxABuf; ++i) {
-            mbar_init(&afull[i], 8);                // the 8 dequant warps that fill it
-            mbar_init(&aempty[i], 2);              // the two issuers (row blocks) that read it
+        for (int i = 0; i < 2 * kMaxABuf; ++i) {
+            mbar_init(&afull[i], 4);               // the 4 dequant warps of the row block
+            mbar_init(&aempty[i], 1);              // the one issuer of the row block that reads it
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&accfull[i], n_iss);
@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     // group-accumulate mode: groups of this CTA counted over all its items
     const int ng_item = p.ngroups / ksplit;       // scale groups per item
     const int bpg = p.group / kKA;                // A buffers per scale group
+    const uint32_t nt8 = static_cast<uint32_t>(nt) * 8u;   // one 64-k token atom (nt x 128 B) >> 4
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t bstage = smem_u32(sB + st.idx * b_stage_bytes);
+                    const uint32_t blo = smem_desc_sw128_lo(smem_u32(sB + st.idx * b_stage_bytes));
                     for (int c = 0; c < chunks; ++c, ++bl) {
                         const uint32_t gc = gbase + static_cast<uint32_t>(bl / bpg);
                         if (static_cast<int>(gc % npar) == h) {
@@ -458,23 +459,22 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                                 ok = false;
                                 break;
                             }
-                            if (!mbar_wait(&afull[ab.idx], ab.phase, abort_flag, status)) {
+                            if (!mbar_wait(&afull[ab.idx * 2 + t], ab.phase, abort_flag, status)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
                             const uint32_t d = tmem + slot * (2 * 16) + static_cast<uint32_t>(t * 16);
                             const uint32_t a0 = tmem + abase_col + ab.idx * 128 + t * 64;
+                            // B: 64-k swizzle atoms 2c and 2c+1, 32 B per 16 k inside each
+                            const uint32_t lo0 = blo + static_cast<uint32_t>(2 * c) * nt8;
+                            const uint32_t lo1 = lo0 + nt8;
 #pragma unroll
-                            for (int k16 = 0; k16 < 8; ++k16) {
-                                // B: 64-k swizzle atom (2c + k16/4), 32 B per 16 k inside it
-                                const uint32_t batom = bstage + static_cast<uint32_t>((2 * c + (k16 >> 2)) * nt * 128 +
-                                                                                      (k16 & 3) * 32);
-                                tc_mma_ts(d, a0 + k16 * 8, smem_desc_sw128(batom), idesc,
-                                          (bin == 0 && k16 == 0) ? 0u : 1u);
-                            }
+                            for (int k16 = 0; k16 < 8; ++k16)
+                                tc_mma_ts_lohi(d, a0 + k16 * 8, (k16 < 4 ? lo0 : lo1) + (k16 & 3) * 2, kSmemDescSw128Hi,
+                                               idesc, (bin == 0 && k16 == 0) ? 0u : 1u);
                             issued = true;
-                            tc_commit(&aempty[ab.idx]);
+                            tc_commit(&aempty[ab.idx * 2 + t]);
                             if (bin == bpg - 1) tc_commit(&gfull[slot]);
                         }
                         ab.next(nabuf);
@@ -511,25 +511,26 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                         ok = false;
                         break;
                     }
-                    const uint32_t bstage = smem_u32(sB + st.idx * b_stage_bytes);
+                    const uint32_t blo = smem_desc_sw128_lo(smem_u32(sB + st.idx * b_stage_bytes));
                     for (int c = 0; c < chunks; ++c, ++bl) {
                         if (n_iss == 2 || (bl & 1) == h) {
-                            if (!mbar_wait(&afull[ab.idx], ab.phase, abort_flag, status)) {
+                            if (!mbar_wait(&afull[ab.idx * 2 + t], ab.phase, abort_flag, status)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
                             const uint32_t a0 = tmem + abase_col + ab.idx * 128 + t * 64;
+                            // B: 64-k swizzle atoms 2c and 2c+1, 32 B per 16 k inside each
+                            const uint32_t lo0 = blo + static_cast<uint32_t>(2 * c) * nt8;
+                            const uint32_t lo1 = lo0 + nt8;
 #pragma unroll
                             for (int k16 = 0; k16 < 8; ++k16) {
-                                // B: 64-k swizzle atom (2c + k16/4), 32 B per 16 k inside it
-                                const uint32_t batom = bstage + static_cast<uint32_t>((2 * c + (k16 >> 2)) * nt * 128 +
-                                                                                      (k16 & 3) * 32);
-                                tc_mma_ts(d, a0 + k16 * 8, smem_desc_sw128(batom), idesc, accumulate);
+                                tc_mma_ts_lohi(d, a0 + k16 * 8, (k16 < 4 ? lo0 : lo1) + (k16 & 3) * 2, kSmemDescSw128Hi,
+                                               idesc, accumulate);
                                 accumulate = 1;
                             }
                             issued = true;
-                            tc_commit(&aempty[ab.idx]);
+                            tc_commit(&aempty[ab.idx * 2 + t]);
                         }
                         ab.next(nabuf);
                     }
@@ -604,7 +605,6 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
         const uint32_t abase = tmem + abase_col + lane_base + static_cast<uint32_t>(blk * 64);
         Ring st, ab, sb;
         bool ok = true;
-        int pending = -1;   // A buffer whose stores are issued but not yet waited for
         const int halves_per_group = p.group / 64;
         for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
             const int u = v / ksplit;
@@ -635,6 +635,14 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     // and stage and scale slots are double-buffered.  Every warp
                     // arrives on the buffers in order, so afull phases complete in
                     // order, which the issuers' parity waits rely on.
+                    // one TMEM A buffer = 128 k = two 64-k halves (scales may differ
+                    // for group 64), this warp's 32 rows of its row block.  The
+                    // buffer's aempty phase is probed before the arithmetic (the
+                    // answer takes ~50-100 cycles); the stores are waited for and
+                    // afull is arrived on at once, which measured faster than
+                    // deferring them past the next buffer.
+                    const uint32_t abar = ab.idx * 2 + blk;   // per row block
+                    const bool a_ready = mbar_test_wait(smem_u32(&aempty[abar]), ab.phase ^ 1u);
                     uint32_t v32[32];
                     if constexpr (BITS == 2) {
                         if (ga) {
@@ -646,14 +654,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                         dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[gi])), v32);
                     }
                     next_half();
-                    if (pending >= 0) {
-                        tc_wait_st();
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&afull[pending]);
-                        pending = -1;
-                    }
-                    if (!mbar_wait(&aempty[ab.idx], ab.phase ^ 1u, abort_flag, status)) {
+                    if (!a_ready && !mbar_wait_bounded(&aempty[abar], ab.phase ^ 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
@@ -670,7 +671,10 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     }
                     next_half();
                     tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v32);
-                    pending = ab.idx;
+                    tc_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&afull[abar]);
                     ab.next(nabuf);
                 }
                 if (!ok) break;
@@ -684,12 +688,6 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 if (lane == 0) mbar_arrive(&sempty[sb.idx]);
                 sb.next(2);
             }
-        }
-        if (pending >= 0) {   // also drains the stores on the abort path
-            tc_wait_st();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&afull[pending]);
         }
     } else if (warp >= kFirstEpilogueWarp && warp < kFirstEpilogueWarp + kEpilogueWarps) {
         // ------------------------------------------------------------ epilogue
@@ -812,8 +810,8 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                         float y0[8], y1[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) y0[i] = y1[i] = 0.0f;
-                        for (int g = 0; g < ng_item && ok; g += 2) {
-                            const int n2 = g + 1 < ng_item ? 2 : 1;
+                        for (int g = 0; g < ng_item && ok; ++g) {
+                            const int n2 = 1;   // one group per wait: releases its slot soonest
                             for (int j = 0; j < n2; ++j) {
                                 const uint32_t gc = gbase + static_cast<uint32_t>(g + j);
                                 if (!mbar_wait(&gfull[gc % kGaSlots], (gc / kGaSlots) & 1u, abort_flag, status)) {
@@ -963,7 +961,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
     const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
-    const int bar_bytes = 8 * (2 * 16 + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2 * kGaSlots) + 16;
+    const int bar_bytes = 8 * (2 * 16 + 4 * kMaxABuf + 4 + 4 + kMaxIssuers + 2 * kGaSlots) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);
     if (ns > 8) ns = 8;
@@ -973,7 +971,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     L.off_w = ns * b_stage;
     L.off_s = L.off_w + ns * w_stage;
     L.off_bar = (L.off_s + s_bytes + 7) & ~7;
-    L.total = L.off_bar + 8 * (2 * ns + 2 * kMaxABuf + 4 + 4 + kMaxIssuers + 2 * kGaSlots) + 16 + 1024;
+    L.total = L.off_bar + 8 * (2 * ns + 4 * kMaxABuf + 4 + 4 + kMaxIssuers + 2 * kGaSlots) + 16 + 1024;
     return L;
 }
 

@@ -91,6 +91,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same condition.  Its result arrives ~100 cycles
+// later; issuing it well before the result is needed hides that latency.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Same, but the thread may sleep in the barrier (up to the hint) until the
 // phase completes, instead of returning at once: waiting warps then take no
 // issue slots from the warps doing the arithmetic.
@@ -264,6 +278,24 @@ __device__ __forceinline__ void tc_ld_32x32b_x8(uint32_t taddr, uint32_t (&v)[8]
 // the 128-byte-swizzled canonical layout: 8-row x 128-byte atoms, rows 128 B
 // apart, 8-row groups 1024 B apart.  `addr` = smem byte address (the atom
 // base must be 1024-byte aligned; K steps inside the atom add 32 B each).
+// The same descriptor as two 32-bit words: the low word holds the start
+// address (addr >> 4) in its low 14 bits, so the descriptor of a tile at
+// addr + off is lo + (off >> 4) while the address stays below 256 KB.
+__device__ __forceinline__ uint32_t smem_desc_sw128_lo(uint32_t addr) { return ((addr >> 4) & 0x3FFFu) | (1u << 16); }
+constexpr uint32_t kSmemDescSw128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+
+// tcgen05.mma kind::f16, A from TMEM, B descriptor given as (lo, hi).
+__device__ __forceinline__ void tc_mma_ts_lohi(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                               uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 bd, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);          // start address
