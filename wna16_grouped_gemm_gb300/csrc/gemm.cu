@@ -371,7 +371,6 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                                                                            : -1;
     // group-accumulate mode: groups of this CTA counted over all its items
     const int ng_item = p.ngroups / ksplit;       // scale groups per item
-    const int bpg = p.group / kKA;                // A buffers per scale group
     const uint32_t nt8 = static_cast<uint32_t>(nt) * 8u;   // one 64-k token atom (nt x 128 B) >> 4
 
     if (warp == kProducerWarp) {
@@ -435,49 +434,48 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
           if (lane == 0 && issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
-            const int npar = n_iss >> 1;
             const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
-            Ring st, ab;
+            // One group per A buffer (group == 128 k); groups (and buffers) are
+            // counted over all items, group g going to parity g % 3, so this
+            // issuer's groups all use group slot h and A buffer h, and the
+            // k-th of them waits for phase k of those barriers.  Counters
+            // instead of divisions: a single thread pays every instruction's
+            // full latency.
+            uint32_t par = 0;    // parity of the current group
+            uint32_t own = 0;    // groups of this parity issued so far
+            const uint32_t d = tmem + static_cast<uint32_t>(h) * (2 * 16) + static_cast<uint32_t>(t * 16);
+            const uint32_t a0 = tmem + abase_col + static_cast<uint32_t>(h) * 128 + t * 64;
+            Ring st;
             bool ok = true;
             bool issued = false;
-            uint32_t gbase = 0;   // groups of the earlier items
-            for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x, gbase += ng_item) {
-                int bl = 0;   // A buffer index within the item
+            for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
                 for (int ks = 0; ks < kps && ok; ++ks) {
                     if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
                         ok = false;
                         break;
                     }
                     const uint32_t blo = smem_desc_sw128_lo(smem_u32(sB + st.idx * b_stage_bytes));
-                    for (int c = 0; c < chunks; ++c, ++bl) {
-                        const uint32_t gc = gbase + static_cast<uint32_t>(bl / bpg);
-                        if (static_cast<int>(gc % npar) == h) {
-                            const uint32_t slot = gc % kGaSlots;
-                            const int bin = bl % bpg;   // buffer within the group
-                            if (bin == 0 && !mbar_wait(&gempty[slot], ((gc / kGaSlots) & 1u) ^ 1u, abort_flag,
-                                                       status)) {
-                                ok = false;
-                                break;
-                            }
-                            if (!mbar_wait(&afull[ab.idx * 2 + t], ab.phase, abort_flag, status)) {
+                    for (int c = 0; c < chunks; ++c) {
+                        if (par == static_cast<uint32_t>(h)) {
+                            if (!mbar_wait(&gempty[h], (own & 1u) ^ 1u, abort_flag, status) ||
+                                !mbar_wait(&afull[h * 2 + t], own & 1u, abort_flag, status)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
-                            const uint32_t d = tmem + slot * (2 * 16) + static_cast<uint32_t>(t * 16);
-                            const uint32_t a0 = tmem + abase_col + ab.idx * 128 + t * 64;
                             // B: 64-k swizzle atoms 2c and 2c+1, 32 B per 16 k inside each
                             const uint32_t lo0 = blo + static_cast<uint32_t>(2 * c) * nt8;
                             const uint32_t lo1 = lo0 + nt8;
 #pragma unroll
                             for (int k16 = 0; k16 < 8; ++k16)
                                 tc_mma_ts_lohi(d, a0 + k16 * 8, (k16 < 4 ? lo0 : lo1) + (k16 & 3) * 2, kSmemDescSw128Hi,
-                                               idesc, (bin == 0 && k16 == 0) ? 0u : 1u);
+                                               idesc, k16 == 0 ? 0u : 1u);
                             issued = true;
-                            tc_commit(&aempty[ab.idx * 2 + t]);
-                            if (bin == bpg - 1) tc_commit(&gfull[slot]);
+                            tc_commit(&aempty[h * 2 + t]);
+                            tc_commit(&gfull[h]);
+                            ++own;
                         }
-                        ab.next(nabuf);
+                        par = par == 2u ? 0u : par + 1u;
                     }
                     if (!ok) break;
                     tc_commit(&empty[st.idx]);
@@ -791,15 +789,14 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 // bf16(scale) * slot in group order.  For 2-bit codes (0 or +-2^j)
                 // code * bf16(scale) is exactly the BF16-rounded dequantised
                 // weight, so this is the same sum as with dequantised weights.
-                // Tiles of at most 8 tokens (decode) read 8 columns per block and
-                // take two groups per TMEM load wait.
-                Ring sb;
-                uint32_t gbase = 0;
+                // Tiles of at most 8 tokens (every decode tile) read only 8
+                // columns per block.
+                Ring sb, gs;   // gs: group slot ring (kGaSlots), advanced per group
                 bool ok = true;
                 auto scale_of = [](uint16_t h) {
                     return __bfloat162float(__float2bfloat16_rn(__half2float(__ushort_as_half(h))));
                 };
-                for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x, gbase += ng_item) {
+                for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
                     const int u = v / ksplit;
                     const int split = v - u * ksplit;
                     const int4 tile = p.tiles[u / p.mt_count];
@@ -810,42 +807,27 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                         float y0[8], y1[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) y0[i] = y1[i] = 0.0f;
-                        for (int g = 0; g < ng_item && ok; ++g) {
-                            const int n2 = 1;   // one group per wait: releases its slot soonest
-                            for (int j = 0; j < n2; ++j) {
-                                const uint32_t gc = gbase + static_cast<uint32_t>(g + j);
-                                if (!mbar_wait(&gfull[gc % kGaSlots], (gc / kGaSlots) & 1u, abort_flag, status)) {
-                                    ok = false;
-                                    break;
-                                }
+                        for (int g = 0; g < ng_item; ++g) {
+                            if (!mbar_wait(&gfull[gs.idx], gs.phase, abort_flag, status)) {
+                                ok = false;
+                                break;
                             }
-                            if (!ok) break;
                             tc_fence_after();
-                            uint32_t d[2][2][8];
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                if (j < n2) {
-                                    const uint32_t col = ((gbase + static_cast<uint32_t>(g + j)) % kGaSlots) * (2 * 16);
-                                    tc_ld_32x32b_x8(tmem + lane_base + col, d[j][0]);
-                                    tc_ld_32x32b_x8(tmem + lane_base + col + 16, d[j][1]);
-                                }
-                            }
+                            uint32_t d0[8], d1[8];
+                            const uint32_t col = gs.idx * (2 * 16);
+                            tc_ld_32x32b_x8(tmem + lane_base + col, d0);
+                            tc_ld_32x32b_x8(tmem + lane_base + col + 16, d1);
                             tc_wait_ld();
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0)
-                                for (int j = 0; j < n2; ++j) mbar_arrive(&gempty[(gbase + g + j) % kGaSlots]);
+                            if (lane == 0) mbar_arrive(&gempty[gs.idx]);
+                            gs.next(kGaSlots);
+                            const float c0 = scale_of(s0row[g]);
+                            const float c1 = scale_of(s1row[g]);
 #pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                if (j < n2) {
-                                    const float c0 = scale_of(s0row[g + j]);
-                                    const float c1 = scale_of(s1row[g + j]);
-#pragma unroll
-                                    for (int i = 0; i < 8; ++i) {
-                                        y0[i] = __fmaf_rn(c0, __uint_as_float(d[j][0][i]), y0[i]);
-                                        y1[i] = __fmaf_rn(c1, __uint_as_float(d[j][1][i]), y1[i]);
-                                    }
-                                }
+                            for (int i = 0; i < 8; ++i) {
+                                y0[i] = __fmaf_rn(c0, __uint_as_float(d0[i]), y0[i]);
+                                y1[i] = __fmaf_rn(c1, __uint_as_float(d1[i]), y1[i]);
                             }
                         }
                         if (!ok) break;
@@ -858,13 +840,12 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i) y0[i] = y1[i] = 0.0f;
                         for (int g = 0; g < ng_item; ++g) {
-                            const uint32_t gc = gbase + static_cast<uint32_t>(g);
-                            const uint32_t col = (gc % kGaSlots) * (2 * 16);
-                            if (!mbar_wait(&gfull[gc % kGaSlots], (gc / kGaSlots) & 1u, abort_flag, status)) {
+                            if (!mbar_wait(&gfull[gs.idx], gs.phase, abort_flag, status)) {
                                 ok = false;
                                 break;
                             }
                             tc_fence_after();
+                            const uint32_t col = gs.idx * (2 * 16);
                             const float c0 = scale_of(s0row[g]);
                             const float c1 = scale_of(s1row[g]);
 #pragma unroll
@@ -881,7 +862,8 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                             }
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&gempty[gc % kGaSlots]);
+                            if (lane == 0) mbar_arrive(&gempty[gs.idx]);
+                            gs.next(kGaSlots);
                         }
                         if (!ok) break;
                         __syncwarp();
