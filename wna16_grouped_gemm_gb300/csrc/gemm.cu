@@ -245,7 +245,10 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t* row, uint32_t xr, i
 __device__ __forceinline__ float swiglu(float g, float u, float L) {
     g = fminf(g, L);
     u = fminf(fmaxf(u, -L), L);
-    return g / (1.0f + expf(-g)) * u;
+    // fast exp / divide: their fp32 errors (a few ulp) are far below the BF16
+    // rounding of h; for very negative g the divisor overflows and the
+    // quotient is 0, as silu's is
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // Position of element k in the interleaved K order (0, 8, 1, 9, ..., 7, 15)

@@ -234,7 +234,10 @@ __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restr
 __device__ __forceinline__ float swiglu_clamped(float g, float u, float L) {
     g = fminf(g, L);
     u = fminf(fmaxf(u, -L), L);
-    return g / (1.0f + expf(-g)) * u;
+    // fast exp / divide: their fp32 errors (a few ulp) are far below the BF16
+    // rounding of h; for very negative g the divisor overflows and the
+    // quotient is 0, as silu's is
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // Split-K epilogue of w13: one block per valid permuted row, threads over n.
