@@ -8,17 +8,20 @@
 //
 // The weights are the M side of the MMA ("swap AB"): a unit is 2 x 128 weight
 // rows (gate+up rows n0.., or 256 consecutive w2 rows) against one token tile
-// of up to NT rows of a single expert.  Per K step:
+// of up to NT rows of a single expert; a work item is a unit and a range of K
+// (split K for decode).  Per 128-k A buffer:
 //
-//   TMA producer (warp 0)   packed INT32 tiles of both weight row blocks and the
-//                           token tile (128B-swizzled BF16) -> smem stage ring
-//   scale loader (warp 2)   the unit's FP16 scales -> smem (transposed)
-//   dequant warps (4..11)   each thread owns one weight row: reads its packed
-//                           words, builds bf16(code*scale) exactly, and writes
-//                           them into a TMEM A buffer with tcgen05.st
-//   MMA issuer (warp 1)     tcgen05.mma kind::f16, A from TMEM, B from smem,
-//                           fp32 accumulators in TMEM (one per row block)
-//   epilogue (warps 4..11)  tcgen05.ld accumulators -> SwiGLU / plain -> BF16
+//   TMA producer (warp 0)      packed INT32 tiles of both weight row blocks and
+//                              the token tile (128B-swizzled BF16) -> smem ring
+//   scale loader (warp 1)      the item's FP16 scales -> smem (cp.async)
+//   dequant warps (4..11)      each thread owns one weight row: reads its packed
+//                              words, builds bf16(code*scale) exactly (or the
+//                              plain code in group-accumulate mode) and writes
+//                              them into a TMEM A buffer with tcgen05.st
+//   MMA issuers (2, 3, 16-19)  tcgen05.mma kind::f16, A from TMEM, B from smem,
+//                              fp32 accumulators (or group slots) in TMEM
+//   epilogue (warps 12..15)    tcgen05.ld -> per-group scaling (group-accumulate
+//                              mode) -> SwiGLU / plain -> BF16, or split-K sums
 //
 // Keeping the dequantised A operand in TMEM means shared memory only carries
 // the packed words and the token tile: the BF16 weights never cross the
@@ -80,13 +83,6 @@ struct Ring {
 
 // ------------------------------------------------------------------ dequant
 //
-// 4-bit fields: a field q placed at mantissa bit `pos` of a float whose
-// exponent field is (150 - pos) reads as 2^(23-pos) + q.  fma(that, s,
-// -(2^(23-pos) + 8) * s) then equals (q - 8) * s = code * s EXACTLY: the
-// product has at most 4 + 11 significant bits and the offset constant at most
-// 13 + 11 <= 24 bits for the positions used (8, 12, 16), so the single
-// rounding of the FMA has nothing to round.  One cvt.rn.bf16x2 then gives the
-// correctly rounded BF16 weights.
 // (a & b) | c in one LOP3.  Written out because with both b and c constant the
 // compiler otherwise emits two logic instructions (one immediate per LOP3),
 // which nearly doubles the integer-pipe work of the dequantisation.
@@ -96,6 +92,13 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
     return d;
 }
 
+// 4-bit fields: a field q placed at mantissa bit `pos` of a float whose
+// exponent field is (150 - pos) reads as 2^(23-pos) + q.  fma(that, s,
+// -(2^(23-pos) + 8) * s) then equals (q - 8) * s = code * s EXACTLY: the
+// product has at most 4 + 11 significant bits and the offset constant at most
+// 13 + 11 <= 24 bits for the positions used (8, 12, 16), so the single
+// rounding of the FMA has nothing to round.  One cvt.rn.bf16x2 then gives the
+// correctly rounded BF16 weights.
 template <int POS>
 __device__ __forceinline__ uint32_t magic_bits() {
     return static_cast<uint32_t>(150 - POS) << 23;
