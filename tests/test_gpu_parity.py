@@ -172,6 +172,21 @@ def test_small_tiles_ragged(moe, oracle):
     gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), "ragged")
 
 
+@pytest.mark.parametrize("K,E", [(512, 8), (1024, 64)])
+def test_decode_tiles_with_9_to_16_rows(moe, oracle, K, E):
+    """2-bit, 16-token tiles (at most 4 rows per expert on average) where a few
+    experts get 9..16 rows: the 16-column path of the group-accumulate
+    epilogue, without (K=512) and with (K=1024, E=64) split K."""
+    w = _small(T=16, K=K, N=256, E=E, topk=2, bits=2)
+    inp = _inputs(w)
+    ids = np.array([0] * 12 + [1] * 14 + [2, 3, 4, 5, 6, 7], np.int32)
+    np.random.default_rng(1).shuffle(ids)
+    inp["ids"] = ids.reshape(16, 2)
+    out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), f"9-16 row tiles K={K}")
+
+
 def test_single_expert_top1(moe, oracle):
     w = _small(T=1, E=1, topk=1, bits=4)
     inp = _inputs(w)

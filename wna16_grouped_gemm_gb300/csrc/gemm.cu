@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&accfull[i], n_iss);
-            mbar_init(&accempty[i], kEpilogueWarps);
+            mbar_init(&accempty[i], n_iss == 2 ? 2 * kEpilogueWarps : kEpilogueWarps);   // + helpers
             mbar_init(&sfull[i], 32);
             mbar_init(&sempty[i], ga ? kEpilogueWarps : kDequantWarps);   // whoever applies the scales
         }
@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 }
             }
         }
-    } else if (issuer >= 0) {
+    } else if (issuer >= 0 && !(n_iss == 2 && warp >= kIssuerWarp2)) {
         // ------------------------------------------------------------ MMA issuers
         // Issuer i serves row block t = i & 1.  One thread can issue a
         // tcgen05.mma only every ~110 cycles, so several issuers keep the tensor
@@ -693,16 +693,25 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 sb.next(2);
             }
         }
-    } else if (warp >= kFirstEpilogueWarp && warp < kFirstEpilogueWarp + kEpilogueWarps) {
+    } else if ((warp >= kFirstEpilogueWarp && warp < kFirstEpilogueWarp + kEpilogueWarps) ||
+               (n_iss == 2 && warp >= kIssuerWarp2)) {
+        // Epilogue warps 12-15; with only 2 issuers (large token tiles) warps
+        // 16-19 are idle as issuers and take the upper half of the token
+        // columns (their lane quarters are warp % 4 as well).
         // ------------------------------------------------------------ epilogue
         // thread = TMEM lane = weight row `row` of both row blocks
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const float L = p.limit;
-        // Writes one item's result for its token columns 0..rows-1;
-        // load(j0, s0, s1) yields both row blocks' sums for columns j0..j0+kEW-1.
-        auto emit = [&](int split, int mt, int rows, int row0, auto&& load) {
+        const bool helper = warp >= kIssuerWarp2;
+        const bool halves = n_iss == 2;   // token columns split between the two warp sets
+        // Writes one item's result for its token columns (all of 0..rows-1, or
+        // this warp set's half of them); load(j0, s0, s1) yields both row
+        // blocks' sums for columns j0..j0+kEW-1.
+        auto emit = [&](int split, int mt, int rows_all, int row0, auto&& load) {
+            const int jbeg = halves && helper ? nt / 2 : 0;
+            const int rows = halves && !helper ? min(rows_all, nt / 2) : rows_all;
             if (ksplit > 1) {
                 // Split K: park this split's fp32 sums for the tile's real token
                 // rows in partial[split][mt][permuted row][256 weight rows]; a
@@ -711,7 +720,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 const int64_t R_rows = p.partial_rows;
                 float* mine = p.partial + ((static_cast<int64_t>(split) * p.mt_count + mt) * R_rows + row0) *
                                               (2 * kRowsPerTile) + row;
-                for (int j0 = 0; j0 < rows; j0 += kEW) {
+                for (int j0 = jbeg; j0 < rows; j0 += kEW) {
                     float s0[kEW], s1[kEW];
                     load(j0, s0, s1);
 #pragma unroll
@@ -728,7 +737,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 // gate = block 0, up = block 1 of the same lane
                 const int n0 = mt * kRowsPerTile + row;
                 const int n = p.h_interleaved ? interleave16(n0) : n0;
-                for (int j0 = 0; j0 < rows; j0 += kEW) {
+                for (int j0 = jbeg; j0 < rows; j0 += kEW) {
                     float g[kEW], uu[kEW];
                     load(j0, g, uu);
 #pragma unroll
@@ -739,7 +748,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 }
             } else {
                 const int m = mt * 2 * kRowsPerTile + row;
-                for (int j0 = 0; j0 < rows; j0 += kEW) {
+                for (int j0 = jbeg; j0 < rows; j0 += kEW) {
                     float y0[kEW], y1[kEW];
                     load(j0, y0, y1);
 #pragma unroll
