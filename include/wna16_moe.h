@@ -178,6 +178,20 @@ WNA16_API int wna16_moe_forward_noalloc(const void* x, const int32_t* topk_ids, 
                                         int group_size, int group_size_w2, int bits, float swiglu_limit,
                                         void* out, void* stream);
 
+/* ---- failure detection check (not part of the method). ----
+ * Every pipeline wait in the GEMM kernels gives up after a bounded time
+ * (2 s), stores WNA16_ERR_DEVICE_TIMEOUT in the workspace status word, makes
+ * the CTA's other waits return, drains its copies and MMAs and frees its
+ * TMEM, so that a stalled pipeline is reported instead of hanging the GPU.
+ * wna16_moe_check_wait_timeout runs one such wait, with a limit of limit_us
+ * microseconds (0 < limit_us <= 5e6), on a barrier that nothing completes,
+ * and so sets the status word of `workspace` (at least 4 bytes, device) to
+ * WNA16_ERR_DEVICE_TIMEOUT; read it with wna16_moe_read_status.  The next
+ * forward on that workspace resets the word.  Asynchronous on `stream`.
+ * Returns WNA16_OK, WNA16_ERR_INVALID_ARG or WNA16_ERR_CUDA. */
+WNA16_API int wna16_moe_check_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_us,
+                                           void* stream);
+
 /* ---- instrumentation (not part of the method): per-stage device times. ----
  * wna16_moe_profile(slots) with slots > 0 makes every later
  * wna16_moe_forward on the calling thread record CUDA events on its stream

@@ -19,7 +19,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = binding.exported_names_in_header()
-    assert len(names) == 12, names
+    assert len(names) == 13, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -97,6 +97,13 @@ def test_stage_entry_points_reject_on_host(lib):
         binding.ERR_WORKSPACE_TOO_SMALL
     assert lib.wna16_moe_combine(A16, A16, 4, 4096, 8, 256, 2048, 2, A16, None, 1 << 40, None) == \
         binding.ERR_INVALID_ARG
+
+
+def test_wait_timeout_check_rejects_on_host(lib):
+    assert lib.wna16_moe_check_wait_timeout(None, 16, 1000, None) == binding.ERR_INVALID_ARG
+    assert lib.wna16_moe_check_wait_timeout(A16, 2, 1000, None) == binding.ERR_INVALID_ARG
+    assert lib.wna16_moe_check_wait_timeout(A16, 16, 0, None) == binding.ERR_INVALID_ARG
+    assert lib.wna16_moe_check_wait_timeout(A16, 16, 10_000_000, None) == binding.ERR_INVALID_ARG
 
 
 def test_profile_read_without_forward_is_an_error(lib):

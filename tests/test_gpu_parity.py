@@ -187,6 +187,23 @@ def test_decode_tiles_with_9_to_16_rows(moe, oracle, K, E):
     gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), f"9-16 row tiles K={K}")
 
 
+def test_stalled_wait_reports_timeout_and_context_survives(moe, oracle):
+    """A bounded device wait that nothing completes (10 ms limit) reports
+    ERR_DEVICE_TIMEOUT in the status word instead of hanging, and the context
+    stays usable: the next forward on the same workspace is correct."""
+    w = synth.get("tiny_w2")
+    inp = _inputs(w)
+    d = gu.to_dev(inp)
+    ws = moe.alloc_workspace(w.T, w.K, w.N, w.E, w.topk, w.bits)
+    moe.check_wait_timeout(ws, 10_000)
+    assert moe.read_status(ws) == moe.ERR_DEVICE_TIMEOUT
+    out = moe.forward(d["x"], d["topk_ids"], d["topk_weights"], d["w13_packed"], d["w13_scales"],
+                      d["w2_packed"], d["w2_scales"], bits=w.bits, group_size=w.g13, group_size_w2=w.g2,
+                      swiglu_limit=w.swiglu_limit, workspace=ws)
+    assert moe.read_status(ws) == moe.OK
+    gu.assert_close(gu.host_bits(out), _oracle_fwd(oracle, w, inp), "after a timed-out wait")
+
+
 def test_single_expert_top1(moe, oracle):
     w = _small(T=1, E=1, topk=1, bits=4)
     inp = _inputs(w)

@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH):
     lib.wna16_moe_w2.argtypes = [P, P, P, I64, I64, I64, I64, I, I, I, P, P, SZ, P]
     lib.wna16_moe_forward_noalloc.restype = I
     lib.wna16_moe_forward_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, I, I, F, P, P]
+    lib.wna16_moe_check_wait_timeout.restype = I
+    lib.wna16_moe_check_wait_timeout.argtypes = [P, SZ, I64, P]
     lib.wna16_moe_profile.restype = I
     lib.wna16_moe_profile.argtypes = [I]
     lib.wna16_moe_profile_read.restype = I
@@ -206,6 +208,13 @@ def profile_read(n: int = 1) -> list[dict]:
     ms = (ctypes.c_float * (5 * n))()
     _check(load_library().wna16_moe_profile_read(ms, n))
     return [dict(zip(STAGES, [float(ms[5 * i + j]) for j in range(5)])) for i in range(n)]
+
+
+def check_wait_timeout(workspace: torch.Tensor, limit_us: int, stream=None) -> None:
+    """Run one bounded device wait that nothing completes; it leaves
+    ERR_DEVICE_TIMEOUT in the workspace status word (see read_status)."""
+    _check(load_library().wna16_moe_check_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                                       int(limit_us), _stream(stream)))
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

@@ -422,6 +422,15 @@ int wna16_moe_read_status(const void* workspace, int* device_status, void* strea
     return WNA16_OK;
 }
 
+int wna16_moe_check_wait_timeout(void* workspace, size_t workspace_bytes, int64_t limit_us, void* stream) {
+    g_err[0] = 0;
+    if (!workspace || workspace_bytes < sizeof(int)) return fail(WNA16_ERR_INVALID_ARG, "workspace too small or NULL");
+    if (limit_us <= 0 || limit_us > 5000000) return fail(WNA16_ERR_INVALID_ARG, "limit_us must be in (0, 5e6]");
+    cudaError_t e = launch_wait_timeout_check(static_cast<int*>(workspace), static_cast<uint64_t>(limit_us) * 1000u,
+                                              static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "wait check kernel launch");
+}
+
 int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_weights, const int32_t* w13_packed,
                       const uint16_t* w13_scales, const int32_t* w2_packed, const uint16_t* w2_scales, int64_t T,
                       int64_t K, int64_t N, int64_t E, int topk, int group_size, int group_size_w2, int bits,

@@ -77,5 +77,7 @@ cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, con
                                     int T, int topk, int K, __nv_bfloat16* out, cudaStream_t stream);
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
                         cudaStream_t stream);
+// One bounded mbarrier wait that nothing completes (device failure-detection check).
+cudaError_t launch_wait_timeout_check(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 }  // namespace wna16

@@ -393,6 +393,24 @@ cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, con
                       out);
 }
 
+// One bounded pipeline wait on a barrier that nothing completes: the wait
+// gives up after limit_ns and reports WNA16_ERR_DEVICE_TIMEOUT in *status,
+// exactly as a stalled GEMM pipeline would.
+__global__ void wait_timeout_check_kernel(int* status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+    mbar_wait_bounded(&bar, 0, &abort_flag, status, false, limit_ns);
+}
+
+cudaError_t launch_wait_timeout_check(int* status, uint64_t limit_ns, cudaStream_t stream) {
+    wait_timeout_check_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
                         cudaStream_t stream) {
     const int64_t n_words = rows * (K * bits / 32);

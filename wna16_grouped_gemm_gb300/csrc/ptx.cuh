@@ -122,12 +122,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 }
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
-// false) when *abort is set by another thread of the CTA, or after
-// kWaitLimitNs, in which case it sets *abort and the status word.  With
+// false) when *abort is set by another thread of the CTA, or after limit_ns
+// (default kWaitLimitNs), in which case it sets *abort and the status word.  With
 // `backoff`, the waiter sleeps briefly between polls so that it does not take
 // issue slots from the warps doing the arithmetic.
 static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                      int* status, bool backoff = false) {
+                                                      int* status, bool backoff = false,
+                                                      uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t a = smem_u32(bar);
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -137,7 +138,7 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t pa
             if (backoff) __nanosleep(128);
         }
         if (*abort) return false;
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
             atomicExch(status, kStatusTimeout);
             return false;
