@@ -204,6 +204,10 @@ WNA16_API int wna16_moe_check_wait_timeout(void* workspace, size_t workspace_byt
 WNA16_API int wna16_moe_profile(int slots);
 WNA16_API int wna16_moe_profile_read(float* ms, int n);
 
+/* Number of kernels the last successful wna16_moe_forward on the calling
+ * thread launched (5, or 6 when w13 is split along K); 0 before any. */
+WNA16_API int wna16_moe_launches_last_forward(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH):
     lib.wna16_moe_forward_noalloc.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I, I, I, F, P, P]
     lib.wna16_moe_check_wait_timeout.restype = I
     lib.wna16_moe_check_wait_timeout.argtypes = [P, SZ, I64, P]
+    lib.wna16_moe_launches_last_forward.restype = I
+    lib.wna16_moe_launches_last_forward.argtypes = []
     lib.wna16_moe_profile.restype = I
     lib.wna16_moe_profile.argtypes = [I]
     lib.wna16_moe_profile_read.restype = I
@@ -215,6 +217,11 @@ def check_wait_timeout(workspace: torch.Tensor, limit_us: int, stream=None) -> N
     ERR_DEVICE_TIMEOUT in the workspace status word (see read_status)."""
     _check(load_library().wna16_moe_check_wait_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
                                                        int(limit_us), _stream(stream)))
+
+
+def launches_last_forward() -> int:
+    """Kernels the last forward on this thread launched."""
+    return int(load_library().wna16_moe_launches_last_forward())
 
 
 def read_status(workspace: torch.Tensor, stream=None) -> int:

@@ -31,6 +31,7 @@ struct StageEvents {
     cudaEvent_t* ev = nullptr;
 };
 thread_local StageEvents g_prof;
+thread_local int g_launches = 0;   // kernels the last wna16_moe_forward on this thread launched
 
 inline void mark(int i, cudaStream_t s) {
     if (g_prof.slots) cudaEventRecord(g_prof.ev[g_prof.next * 6 + i], s);
@@ -497,8 +498,11 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     mark(5, s);
     mark_done();
+    g_launches = 5 + (p13.gp.ksplit > 1 ? 1 : 0);
     return WNA16_OK;
 }
+
+int wna16_moe_launches_last_forward(void) { return g_launches; }
 
 int wna16_moe_profile(int slots) {
     g_err[0] = 0;
