@@ -169,6 +169,20 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ CPU oracle timing
 
+def cpu_model() -> str:
+    """The host CPU's model name (or the architecture when /proc does not say)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
+
+
 def time_oracle(w: synth.Workload, inp: dict, budget_s: float, min_runs: int = 1, max_tokens: int | None = None):
     """Run the oracle forward on a bounded token sample; returns (tokens/s, sample text, cores, seconds)."""
     import oracle
@@ -256,7 +270,7 @@ def run_reference(args, w, rank, world, dist):
                 ms_per_step=1000.0 * total / args.steps, higher_is_better=True, scaling="weak", vs_baseline=None,
                 dtype="f64", data="synthetic", config=workload_config(w),
                 cpu_baseline=dict(value=value, unit="tokens/s", cores=oracle.num_threads(), kind="oracle",
-                                  sample=sample),
+                                  sample=sample, cpu=cpu_model()),
                 e2e=dict(value=value, unit="tokens/s", h2d_bytes_per_step=0, d2h_bytes_per_step=0))
     print(json.dumps(line))
     if dist:
@@ -413,7 +427,8 @@ def main():
         if not args.no_cpu_baseline:
             max_tok = None if w.T <= 16 else 8
             rate, sample, cores, _ = time_oracle(w, inp, args.oracle_seconds, 1, max_tok)
-            line["cpu_baseline"] = dict(value=rate, unit="tokens/s", cores=cores, kind="oracle", sample=sample)
+            line["cpu_baseline"] = dict(value=rate, unit="tokens/s", cores=cores, kind="oracle", sample=sample,
+                                        cpu=cpu_model())
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()
