@@ -74,11 +74,15 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     pdl_trigger();
     if (tid == 0) *status = kStatusOk;
 
-    const int per_warp = (((R + kRouteWarps - 1) / kRouteWarps) + 31) & ~31;
+    // W warps hold slots (32 each, more once R > 32 * kRouteWarps); the
+    // per-expert passes below walk only their W count rows
+    const int W = max(1, min(kRouteWarps, (R + 31) / 32));
+    const int per_warp = (((R + W - 1) / W) + 31) & ~31;
     const int f0 = warp * per_warp;
     const int f1 = min(R, f0 + per_warp);
     int* my = cnt + warp * E;
-    for (int e = lane; e < E; e += 32) my[e] = 0;
+    if (warp < W)
+        for (int e = lane; e < E; e += 32) my[e] = 0;
     __syncwarp();
 
     bool bad = false;
@@ -101,7 +105,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 
     int c = 0;
     if (tid < E) {
-        for (int w = 0; w < kRouteWarps; ++w) {
+        for (int w = 0; w < W; ++w) {
             const int v = cnt[w * E + tid];
             cnt[w * E + tid] = c;
             c += v;
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         counts[tid] = c;
         offsets[tid] = off;
         for (int j = 0; j < ntl; ++j) tiles[toff + j] = make_int4(tid, off + j * nt, min(nt, c - j * nt), 0);
-        for (int w = 0; w < kRouteWarps; ++w) cnt[w * E + tid] += off;
+        for (int w = 0; w < W; ++w) cnt[w * E + tid] += off;
     }
     if (tid == 0) {
         offsets[E] = total;
@@ -207,8 +211,8 @@ __global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t bl
 __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restrict__ w, const int* __restrict__ inv,
                                int topk, int vec_per_row, uint4* __restrict__ out) {
     pdl_wait();
-    const int t = blockIdx.y;
-    const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    const int t = blockIdx.x;
+    const int v = blockIdx.y * blockDim.x + threadIdx.x;
     if (v >= vec_per_row) return;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < topk; ++j) {
@@ -240,28 +244,43 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float L) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// Split-K epilogue of w13: one block per valid permuted row, threads over n.
-__global__ void finalize_w13_kernel(const float* __restrict__ partial, int ksplit, int R, const int* __restrict__ offsets_end,
+// Split-K epilogue of w13: blockIdx.x = permuted row (valid rows only), each
+// thread 4 consecutive n; all KS partial loads of a thread are issued before
+// the first is used, and the splits are added in ascending order.
+template <int KS>
+__global__ void finalize_w13_kernel(const float* __restrict__ partial, int R, const int* __restrict__ offsets_end,
                                     int N, float L, int interleave, __nv_bfloat16* __restrict__ h) {
     pdl_wait();
     pdl_trigger();
     const int r = blockIdx.x;
     if (r >= *offsets_end) return;
+    const int n0 = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+    if (n0 >= N) return;
     const int mtc = N / 128;
-    for (int n = threadIdx.x; n < N; n += blockDim.x) {
-        const int mt = n >> 7, i = n & 127;
-        float g = 0.f, u = 0.f;
-        for (int s = 0; s < ksplit; ++s) {
-            const float* q = partial + ((static_cast<int64_t>(s) * mtc + mt) * R + r) * 256;
-            g += q[i];
-            u += q[128 + i];
-        }
+    const float* q = partial + (static_cast<int64_t>(n0 >> 7) * R + r) * 256 + (n0 & 127);
+    const int64_t split_stride = static_cast<int64_t>(mtc) * R * 256;
+    float4 g[KS], u[KS];
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+        g[s] = __ldg(reinterpret_cast<const float4*>(q + s * split_stride));
+        u[s] = __ldg(reinterpret_cast<const float4*>(q + s * split_stride + 128));
+    }
+    float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+        gs[0] += g[s].x; gs[1] += g[s].y; gs[2] += g[s].z; gs[3] += g[s].w;
+        us[0] += u[s].x; us[1] += u[s].y; us[2] += u[s].z; us[3] += u[s].w;
+    }
+    __nv_bfloat16* hr = h + static_cast<int64_t>(r) * N;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int n = n0 + e;
         int col = n;
         if (interleave) {
-            const int e = n & 15;
-            col = (n & ~15) | (e < 8 ? 2 * e : 2 * (e - 8) + 1);
+            const int b = n & 15;
+            col = (n & ~15) | (b < 8 ? 2 * b : 2 * (b - 8) + 1);
         }
-        h[static_cast<int64_t>(r) * N + col] = __float2bfloat16_rn(swiglu_clamped(g, u, L));
+        hr[col] = __float2bfloat16_rn(swiglu_clamped(gs[e], us[e], L));
     }
 }
 
@@ -281,32 +300,64 @@ __global__ void finalize_w2_kernel(const float* __restrict__ partial, int ksplit
 
 // Combine straight from the w2 split partial sums: y is rounded to BF16 exactly
 // where the unsplit path stores it, then weighted and summed (j ascending).
-__global__ void combine_partials_kernel(const float* __restrict__ partial, int ksplit, int R,
-                                        const float* __restrict__ w, const int* __restrict__ inv, int topk, int K,
+// The lanes of a warp fetch up to 32 (slot row, weight) pairs at once and
+// pass them round by shuffles; the KS partial loads of a slot are issued
+// together.
+template <int KS>
+__global__ void combine_partials_kernel(const float* __restrict__ partial, int R, const float* __restrict__ w,
+                                        const int* __restrict__ inv, int topk, int K,
                                         __nv_bfloat16* __restrict__ out) {
     pdl_wait();
-    const int t = blockIdx.y;
-    const int m0 = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (m0 >= K) return;
+    const int t = blockIdx.x;
+    const int lane = threadIdx.x & 31;
+    const int m0 = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+    const bool active = m0 < K;   // warp-uniform: K / 4 is a multiple of 32
     const int mtc = K / 256;
+    const int64_t split_stride = static_cast<int64_t>(mtc) * R * 256;
+    const float* col = partial + static_cast<int64_t>(m0 >> 8) * R * 256 + (m0 & 255);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < topk; ++j) {
-        const int r = inv[t * topk + j];
-        if (r < 0) continue;
-        const float wj = w[t * topk + j];
-        float ysum[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s = 0; s < ksplit; ++s) {
-            const float4 q = *reinterpret_cast<const float4*>(
-                partial + ((static_cast<int64_t>(s) * mtc + (m0 >> 8)) * R + r) * 256 + (m0 & 255));
-            ysum[0] += q.x;
-            ysum[1] += q.y;
-            ysum[2] += q.z;
-            ysum[3] += q.w;
+    for (int j0 = 0; j0 < topk; j0 += 32) {
+        const int jn = min(32, topk - j0);
+        int rl = -1;
+        float wl = 0.f;
+        if (lane < jn) {
+            rl = inv[t * topk + j0 + lane];
+            wl = w[t * topk + j0 + lane];
         }
+        // JB slots per round: their loads are all in flight before the first sum
+        constexpr int JB = KS <= 4 ? 4 : 2;
+        for (int j = 0; j < jn; j += JB) {
+            int r[JB];
+            float wj[JB];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            acc[i] = __fmaf_rn(wj, __bfloat162float(__float2bfloat16_rn(ysum[i])), acc[i]);
+            for (int b = 0; b < JB; ++b) {
+                r[b] = __shfl_sync(0xffffffffu, rl, (j + b) & 31);
+                wj[b] = __shfl_sync(0xffffffffu, wl, (j + b) & 31);
+                if (j + b >= jn || !active) r[b] = -1;
+            }
+            float4 q[JB][KS];
+#pragma unroll
+            for (int b = 0; b < JB; ++b)
+#pragma unroll
+                for (int s = 0; s < KS; ++s)
+                    q[b][s] = r[b] >= 0 ? __ldg(reinterpret_cast<const float4*>(
+                                              col + s * split_stride + static_cast<int64_t>(r[b]) * 256))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int b = 0; b < JB; ++b) {
+                if (r[b] < 0) continue;
+                float ysum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int s = 0; s < KS; ++s) {
+                    ysum[0] += q[b][s].x; ysum[1] += q[b][s].y; ysum[2] += q[b][s].z; ysum[3] += q[b][s].w;
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    acc[i] = __fmaf_rn(wj[b], __bfloat162float(__float2bfloat16_rn(ysum[i])), acc[i]);
+            }
+        }
     }
+    if (!active) return;
     __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + static_cast<int64_t>(t) * K + m0);
     o[0] = __floats2bfloat162_rn(acc[0], acc[1]);
     o[1] = __floats2bfloat162_rn(acc[2], acc[3]);
@@ -366,7 +417,7 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const i
     if (T == 0) return cudaSuccess;
     const int vpr = K / 8;
     const int threads = 128;
-    dim3 grid((vpr + threads - 1) / threads, T);
+    const dim3 grid(T, (vpr + threads - 1) / threads);
     return launch_pdl(combine_kernel, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y), weights, inv,
                       topk, vpr, reinterpret_cast<uint4*>(out));
 }
@@ -374,8 +425,17 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const i
 cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
                                 int interleave, __nv_bfloat16* h, cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
-    return launch_pdl(finalize_w13_kernel, dim3(R), dim3(256), 0, stream, partial, ksplit, R, offsets_end, N, limit,
-                      interleave, h);
+    const int threads = 128;
+    const dim3 grid(R, (N / 4 + threads - 1) / threads);
+    switch (ksplit) {
+        case 2: return launch_pdl(finalize_w13_kernel<2>, grid, dim3(threads), 0, stream, partial, R, offsets_end, N,
+                                  limit, interleave, h);
+        case 4: return launch_pdl(finalize_w13_kernel<4>, grid, dim3(threads), 0, stream, partial, R, offsets_end, N,
+                                  limit, interleave, h);
+        case 8: return launch_pdl(finalize_w13_kernel<8>, grid, dim3(threads), 0, stream, partial, R, offsets_end, N,
+                                  limit, interleave, h);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const int* offsets_end, int K,
@@ -388,9 +448,16 @@ cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, con
                                     int T, int topk, int K, __nv_bfloat16* out, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const int threads = 128;
-    dim3 grid((K / 4 + threads - 1) / threads, T);
-    return launch_pdl(combine_partials_kernel, grid, dim3(threads), 0, stream, partial, ksplit, R, weights, inv, topk, K,
-                      out);
+    const dim3 grid(T, (K / 4 + threads - 1) / threads);
+    switch (ksplit) {
+        case 2: return launch_pdl(combine_partials_kernel<2>, grid, dim3(threads), 0, stream, partial, R, weights, inv,
+                                  topk, K, out);
+        case 4: return launch_pdl(combine_partials_kernel<4>, grid, dim3(threads), 0, stream, partial, R, weights, inv,
+                                  topk, K, out);
+        case 8: return launch_pdl(combine_partials_kernel<8>, grid, dim3(threads), 0, stream, partial, R, weights, inv,
+                                  topk, K, out);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 // One bounded pipeline wait on a barrier that nothing completes: the wait
