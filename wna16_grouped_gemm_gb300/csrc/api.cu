@@ -97,6 +97,7 @@ struct Layout {
     int64_t units13 = 0, units2 = 0;      // largest possible unit counts of the two GEMMs
     size_t status = 0, n_tiles = 0, counts = 0, offsets = 0, perm = 0, inv = 0, tiles = 0, xp = 0, h = 0, y = 0;
     size_t partial = 0;
+    size_t csum13 = 0, csum2 = 0;         // offset-code corrections (2-bit, 16-token tiles): [groups][R]
     size_t total = 0;
 };
 
@@ -126,6 +127,10 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.h = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * N);
     L.y = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
     L.partial = o;  o = align_up(o + sizeof(float) * partial_floats);
+    // group-accumulate mode (2-bit, 16-token tiles, group 128) with offset codes
+    const bool ga = bits == 2 && L.nt == 16;
+    L.csum13 = o;   o = align_up(o + (ga ? sizeof(float) * L.R * (K / 128) : 0));
+    L.csum2 = o;    o = align_up(o + (ga ? sizeof(float) * L.R * (N / 128) : 0));
     L.total = o;
     return L;
 }
@@ -274,7 +279,7 @@ struct GemmPlan {
 
 int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uint16_t* wscales, const void* b_src,
               void* out, int64_t K, int64_t N, int64_t E, int group, float limit, const Layout& L, void* ws,
-              bool h_interleaved = false) {
+              bool h_interleaved = false, const float* csum = nullptr) {
     DevInfo dev;
     if (int rc = device_info(dev)) return rc;
     const int64_t kred = w13 ? K : N;
@@ -337,6 +342,8 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.dequant_warps = 8;
     // group-accumulate mode: one A buffer per scale group (group == 128 k)
     gp.ga = (bits == 2 && nt == 16 && group == 128) ? 1 : 0;
+    // offset codes when the caller provides the token corrections
+    gp.csum = gp.ga ? csum : nullptr;
     if (gp.ga) {
         gp.n_issuers = 6;
         gp.nacc = 1;
@@ -463,11 +470,16 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     // 2-bit weights are consumed in the interleaved 16-k order: x is gathered
     // and h is written in that order (w2's input), y and out are not affected.
     const bool il = bits == 2;
+    // Group-accumulate mode takes offset codes when the token operand's
+    // corrections are written with it: by the gather for w13, by the split-K
+    // finalize (which writes h) for w2.
     if (int rc = plan_gemm(p13, true, bits, w13_packed, w13_scales, at<void>(workspace, L.xp),
-                           at<void>(workspace, L.h), K, N, E, group_size, swiglu_limit, L, workspace, il))
+                           at<void>(workspace, L.h), K, N, E, group_size, swiglu_limit, L, workspace, il,
+                           at<float>(workspace, L.csum13)))
         return rc;
     if (int rc = plan_gemm(p2, false, bits, w2_packed, w2_scales, at<void>(workspace, L.h), at<void>(workspace, L.y),
-                           K, N, E, g2, swiglu_limit, L, workspace))
+                           K, N, E, g2, swiglu_limit, L, workspace, false,
+                           p13.gp.ksplit > 1 ? at<float>(workspace, L.csum2) : nullptr))
         return rc;
 
     mark(0, s);
@@ -475,14 +487,16 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     mark(1, s);
     cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
-                                  static_cast<int>(K), il ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp), s);
+                                  static_cast<int>(K), il ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
+                                  p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     mark(2, s);
     if (int rc = launch_plan(p13, s)) return rc;
     if (p13.gp.ksplit > 1) {   // split K: fixed-order sum of the splits + SwiGLU -> h
         e = launch_finalize_w13(at<float>(workspace, L.partial), p13.gp.ksplit, static_cast<int>(L.R),
                                 at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, il ? 1 : 0,
-                                at<__nv_bfloat16>(workspace, L.h), s);
+                                at<__nv_bfloat16>(workspace, L.h), p2.gp.csum ? at<float>(workspace, L.csum2) : nullptr,
+                                s);
         if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
     }
     mark(3, s);
@@ -593,18 +607,19 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmPlan p13;
     if (int rc = plan_gemm(p13, true, bits, w13_packed, w13_scales, at<void>(workspace, L.xp), h_out, K, N, E,
-                           group_size, swiglu_limit, L, workspace))
+                           group_size, swiglu_limit, L, workspace, false, at<float>(workspace, L.csum13)))
         return rc;
     if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
     cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
-                                  static_cast<int>(K), bits == 2 ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp), s);
+                                  static_cast<int>(K), bits == 2 ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
+                                  p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     if (int rc = launch_plan(p13, s)) return rc;
     if (p13.gp.ksplit > 1) {
         e = launch_finalize_w13(at<float>(workspace, L.partial), p13.gp.ksplit, static_cast<int>(L.R),
                                 at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, 0,
-                                static_cast<__nv_bfloat16*>(h_out), s);
+                                static_cast<__nv_bfloat16*>(h_out), nullptr, s);
         if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
     }
     return WNA16_OK;

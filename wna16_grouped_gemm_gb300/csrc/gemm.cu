@@ -195,14 +195,43 @@ __device__ __forceinline__ void dequant_word2_codes(uint32_t w, uint32_t* o) {
     o[7] = bf2_fma(and_or(w12, 0x000C000Cu, kBf2Magic), kBf2Quarter, kBf2Neg34);   // fields 7, 15
 }
 
-// 64 consecutive k of one row -> 32 bf16x2 plain 2-bit codes (same layout as
-// dequant_chunk<2>).
+// Offset codes (group-accumulate mode with a per-token correction): the field
+// is OR-ed into a magic number whose exponent makes its weight 1, so the BF16
+// reads off + q with off = 128, 32 or 8 for mantissa bits 0-1, 2-3 or 4-5,
+// one LOP3 per pair and no arithmetic.  With code = q - 2 the MMA sums
+// sum_k (code_k + off_k + 2) x_k; the epilogue subtracts the token's
+// sum_k (off_k + 2) x_k over the group, computed where the token operand is
+// written.  By k mod 8 the weight off + 2 is 130, 34, 10, 130, 34, 10, 130, 34.
+constexpr uint32_t kBf2Magic32 = 0x42004200u;   // (32.0, 32.0)
+constexpr uint32_t kBf2Magic8 = 0x41004100u;    // (8.0, 8.0)
+__device__ __forceinline__ void offset_word2_codes(uint32_t w, uint32_t* o) {
+    const uint32_t w6 = w >> 6, w12 = w >> 12;
+    o[0] = and_or(w, 0x00030003u, kBf2Magic);      // fields 0, 8:  128 + q
+    o[1] = and_or(w, 0x000C000Cu, kBf2Magic32);    // fields 1, 9:  32 + q
+    o[2] = and_or(w, 0x00300030u, kBf2Magic8);     // fields 2, 10: 8 + q
+    o[3] = and_or(w6, 0x00030003u, kBf2Magic);     // fields 3, 11
+    o[4] = and_or(w6, 0x000C000Cu, kBf2Magic32);   // fields 4, 12
+    o[5] = and_or(w6, 0x00300030u, kBf2Magic8);    // fields 5, 13
+    o[6] = and_or(w12, 0x00030003u, kBf2Magic);    // fields 6, 14
+    o[7] = and_or(w12, 0x000C000Cu, kBf2Magic32);  // fields 7, 15
+}
+
+// 64 consecutive k of one row -> 32 bf16x2 plain 2-bit codes, or offset codes
+// with OFFSET (same layout as dequant_chunk<2>).
+template <bool OFFSET>
 __device__ __forceinline__ void codes_chunk2(const uint8_t* row, uint32_t xr, int chunk, uint32_t (&o)[32]) {
     const uint4 v = *reinterpret_cast<const uint4*>(row + ((static_cast<uint32_t>(chunk) ^ xr) << 4));
-    dequant_word2_codes(v.x, o + 0);
-    dequant_word2_codes(v.y, o + 8);
-    dequant_word2_codes(v.z, o + 16);
-    dequant_word2_codes(v.w, o + 24);
+    if constexpr (OFFSET) {
+        offset_word2_codes(v.x, o + 0);
+        offset_word2_codes(v.y, o + 8);
+        offset_word2_codes(v.z, o + 16);
+        offset_word2_codes(v.w, o + 24);
+    } else {
+        dequant_word2_codes(v.x, o + 0);
+        dequant_word2_codes(v.y, o + 8);
+        dequant_word2_codes(v.z, o + 16);
+        dequant_word2_codes(v.w, o + 24);
+    }
 }
 
 // One 4-bit word (8 consecutive k) -> 4 bf16x2.
@@ -276,7 +305,7 @@ __device__ __forceinline__ void unit_rows(const GemmParams& p, int e, int mt, in
 
 }  // namespace
 
-template <int BITS, bool W13, int DW, bool GA>
+template <int BITS, bool W13, int DW, int GA>
 __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_b,
                         const GemmParams p) {
@@ -301,9 +330,12 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     const int nabuf = p.nabuf;
     const int nacc = p.nacc;
     const int n_iss = p.n_issuers;
-    static_assert(!GA || BITS == 2, "group-accumulate mode: 2-bit codes");
+    static_assert(GA == 0 || BITS == 2, "group-accumulate mode: 2-bit codes");
     static_assert(DW == 8, "8 dequant warps: one per row block and TMEM lane quarter");
-    constexpr bool ga = GA;   // group-accumulate mode: see the issuer and epilogue sections
+    // group-accumulate mode (GA 1 or 2; see the issuer and epilogue sections),
+    // GA 2 with offset codes and per-token corrections (p.csum)
+    constexpr bool ga = GA != 0;
+    constexpr bool goff = GA == 2;
 
     uint8_t* sB = smem + p.off_b;
     uint8_t* sW = smem + p.off_w;
@@ -436,7 +468,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
         // h = i >> 1 takes the groups g with g % 3 == h, and every group is
         // accumulated from zero into a slot of kGaSlots that the epilogue warps
         // scale and add up.
-        if constexpr (GA) {
+        if constexpr (ga) {
           if (lane == 0 && issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
@@ -631,26 +663,20 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 const uint8_t* wrow = sW + st.idx * 2 * w_tile_bytes + blk * w_tile_bytes + row * pitch;
                 for (int c = 0; c < chunks; ++c) {
                     // one TMEM A buffer = 128 k = two 64-k halves (scales may differ
-                    // for group 64).  A TMEM store takes hundreds of cycles to
-                    // complete, so the wait for a buffer's stores (and its afull
-                    // arrival) is deferred until the first half of the next buffer
-                    // has been dequantised.  Nothing waited on in between depends on
-                    // the pending buffer: its aempty wait comes after the arrival,
-                    // and stage and scale slots are double-buffered.  Every warp
-                    // arrives on the buffers in order, so afull phases complete in
-                    // order, which the issuers' parity waits rely on.
-                    // one TMEM A buffer = 128 k = two 64-k halves (scales may differ
                     // for group 64), this warp's 32 rows of its row block.  The
                     // buffer's aempty phase is probed before the arithmetic (the
                     // answer takes ~50-100 cycles); the stores are waited for and
                     // afull is arrived on at once, which measured faster than
-                    // deferring them past the next buffer.
+                    // deferring them past the next buffer.  Every warp arrives on
+                    // the buffers in order, so afull phases complete in order.
                     const uint32_t abar = ab.idx * 2 + blk;   // per row block
                     const bool a_ready = mbar_test_wait(smem_u32(&aempty[abar]), ab.phase ^ 1u);
                     uint32_t v32[32];
                     if constexpr (BITS == 2) {
-                        if (ga) {
-                            codes_chunk2(wrow, xr, 2 * c, v32);
+                        if constexpr (goff) {
+                            codes_chunk2<true>(wrow, xr, 2 * c, v32);
+                        } else if (ga) {
+                            codes_chunk2<false>(wrow, xr, 2 * c, v32);
                         } else {
                             dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[gi])), v32);
                         }
@@ -665,8 +691,10 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     tc_fence_after();
                     tc_st_32x32b_x32(abase + ab.idx * 128, v32);
                     if constexpr (BITS == 2) {
-                        if (ga) {
-                            codes_chunk2(wrow, xr, 2 * c + 1, v32);
+                        if constexpr (goff) {
+                            codes_chunk2<true>(wrow, xr, 2 * c + 1, v32);
+                        } else if (ga) {
+                            codes_chunk2<false>(wrow, xr, 2 * c + 1, v32);
                         } else {
                             dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[gi])), v32);
                         }
@@ -797,7 +825,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 }
             }
         };
-        if constexpr (GA) {
+        if constexpr (ga) {
             {
                 // Group-accumulate mode (2-bit codes, 16-token tiles): every group's
                 // code sums arrive in a TMEM slot; this row's sums add
@@ -805,8 +833,12 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 // code * bf16(scale) is exactly the BF16-rounded dequantised
                 // weight, so this is the same sum as with dequantised weights.
                 // Tiles of at most 8 tokens (every decode tile) read only 8
-                // columns per block.
+                // columns per block.  With offset codes the slot holds
+                // sum (code + off + 2) x; the token's correction
+                // sum (off + 2) x over the group (csum[group][permuted row]) is
+                // subtracted first, the same for both row blocks.
                 Ring sb, gs;   // gs: group slot ring (kGaSlots), advanced per group
+                const int R_rows = p.partial_rows;
                 bool ok = true;
                 auto scale_of = [](uint16_t h) {
                     return __bfloat162float(__float2bfloat16_rn(__half2float(__ushort_as_half(h))));
@@ -818,11 +850,17 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
                     const uint16_t* s0row = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + row * ng_item;
                     const uint16_t* s1row = s0row + kRowsPerTile * ng_item;
+                    // corrections of this item's groups for the tile's token rows
+                    const float* crow = goff ? p.csum + static_cast<int64_t>(split * ng_item) * R_rows + tile.y : nullptr;
                     if (tile.z <= 8) {
                         float y0[8], y1[8];
 #pragma unroll
                         for (int i = 0; i < 8; ++i) y0[i] = y1[i] = 0.0f;
                         for (int g = 0; g < ng_item; ++g) {
+                            float cs[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                cs[i] = goff && i < tile.z ? __ldg(crow + static_cast<int64_t>(g) * R_rows + i) : 0.0f;
                             if (!mbar_wait(&gfull[gs.idx], gs.phase, abort_flag, status)) {
                                 ok = false;
                                 break;
@@ -841,8 +879,8 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                             const float c1 = scale_of(s1row[g]);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
-                                y0[i] = __fmaf_rn(c0, __uint_as_float(d0[i]), y0[i]);
-                                y1[i] = __fmaf_rn(c1, __uint_as_float(d1[i]), y1[i]);
+                                y0[i] = __fmaf_rn(c0, __uint_as_float(d0[i]) - cs[i], y0[i]);
+                                y1[i] = __fmaf_rn(c1, __uint_as_float(d1[i]) - cs[i], y1[i]);
                             }
                         }
                         if (!ok) break;
@@ -865,14 +903,20 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                             const float c1 = scale_of(s1row[g]);
 #pragma unroll
                             for (int q = 0; q < 16; q += 8) {
+                                float cs[8];
+#pragma unroll
+                                for (int i = 0; i < 8; ++i)
+                                    cs[i] = goff && q + i < tile.z
+                                                ? __ldg(crow + static_cast<int64_t>(g) * R_rows + q + i)
+                                                : 0.0f;
                                 uint32_t d0[8], d1[8];
                                 tc_ld_32x32b_x8(tmem + lane_base + col + q, d0);
                                 tc_ld_32x32b_x8(tmem + lane_base + col + 16 + q, d1);
                                 tc_wait_ld();
 #pragma unroll
                                 for (int i = 0; i < 8; ++i) {
-                                    y0[q + i] = __fmaf_rn(c0, __uint_as_float(d0[i]), y0[q + i]);
-                                    y1[q + i] = __fmaf_rn(c1, __uint_as_float(d1[i]), y1[q + i]);
+                                    y0[q + i] = __fmaf_rn(c0, __uint_as_float(d0[i]) - cs[i], y0[q + i]);
+                                    y1[q + i] = __fmaf_rn(c1, __uint_as_float(d1[i]) - cs[i], y1[q + i]);
                                 }
                             }
                             tc_fence_before();
@@ -972,7 +1016,7 @@ GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
     return L;
 }
 
-template <int BITS, bool W13, int DW, bool GA>
+template <int BITS, bool W13, int DW, int GA>
 static cudaError_t launch_impl(const CUtensorMap& tm_w, const CUtensorMap& tm_b, const GemmParams& p, int grid,
                                int smem_bytes, cudaStream_t stream) {
     auto kern = grouped_gemm_kernel<BITS, W13, DW, GA>;
@@ -991,9 +1035,10 @@ static cudaError_t launch_dw(const CUtensorMap& tm_w, const CUtensorMap& tm_b, c
                              int smem_bytes, cudaStream_t stream) {
     if (p.dequant_warps != 8) return cudaErrorInvalidValue;
     if constexpr (BITS == 2) {
-        if (p.ga) return launch_impl<BITS, W13, 8, true>(tm_w, tm_b, p, grid, smem_bytes, stream);
+        if (p.ga && p.csum) return launch_impl<BITS, W13, 8, 2>(tm_w, tm_b, p, grid, smem_bytes, stream);
+        if (p.ga) return launch_impl<BITS, W13, 8, 1>(tm_w, tm_b, p, grid, smem_bytes, stream);
     }
-    return launch_impl<BITS, W13, 8, false>(tm_w, tm_b, p, grid, smem_bytes, stream);
+    return launch_impl<BITS, W13, 8, 0>(tm_w, tm_b, p, grid, smem_bytes, stream);
 }
 
 cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, const CUtensorMap& tm_b,

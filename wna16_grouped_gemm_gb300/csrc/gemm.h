@@ -37,6 +37,9 @@ struct GemmParams {
     int partial_rows;           // rows of the permuted token order (R)
     int h_interleaved;          // w13: store h columns in the interleaved 16-k order (2-bit w2 input)
     int scale_copy_bytes;       // 16, 8 or 4: cp.async size for the scale rows; 0: plain loads
+    const float* csum;          // GA mode with offset codes: per scale group and permuted token row,
+                                // sum_k w(k) b[row, k] with w(k) = 130, 34, 10, 130, 34, 10, 130, 34
+                                // by k mod 8 ([ngroups][partial_rows]); null: plain codes
 };
 
 struct GemmSmem {
@@ -57,8 +60,10 @@ int set_error(int code, const char* fmt, ...);
 // Routing / gather / combine / pack kernels (kernels.cu).
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
                          int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream);
+// With csum (2-bit interleaved order only, group 128): also the offset-code
+// corrections of the gathered rows, csum[g * R + i] = sum over group g of w(k) x.
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
-                          int K, int interleave, __nv_bfloat16* xp, cudaStream_t stream);
+                          int K, int interleave, __nv_bfloat16* xp, float* csum, cudaStream_t stream);
 // dst[i, :] = src[i, :] with every 16-element block in the interleaved K order
 // (0, 8, 1, 9, ..., 7, 15) (or back, with inverse = 1).
 cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
@@ -66,9 +71,10 @@ cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
                            __nv_bfloat16* out, cudaStream_t stream);
 // Split-K epilogues (partial sums [ksplit][mt][R][256] fp32, rows < offsets_end):
-//   h[r, n] = bf16(swiglu(sum_s gate, sum_s up)) (column n at its interleaved position if `interleave`)
+//   h[r, n] = bf16(swiglu(sum_s gate, sum_s up)) (column n at its interleaved position if `interleave`),
+//   and with csum the offset-code corrections of h for w2 (group 128), csum[g * R + r]
 cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
-                                int interleave, __nv_bfloat16* h, cudaStream_t stream);
+                                int interleave, __nv_bfloat16* h, float* csum, cudaStream_t stream);
 //   y[r, m] = bf16(sum_s partial)
 cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const int* offsets_end, int K,
                                __nv_bfloat16* y, cudaStream_t stream);

@@ -169,11 +169,38 @@ __device__ __forceinline__ void deinterleave_block(const uint4& a, const uint4& 
     hi.w = __byte_perm(b.z, b.w, 0x7632);
 }
 
+// Weight of element k in the offset-code correction of the grouped GEMM's
+// group-accumulate mode: off(k) + 2 for the magic offset off = 128, 32, 8 of
+// the code field's mantissa position, i.e. 130, 34, 10 for (k mod 8) mod 3 =
+// 0, 1, 2.
+__device__ __forceinline__ float offset_weight(int k) {
+    const int c = (k & 7) % 3;
+    return c == 0 ? 130.0f : (c == 1 ? 34.0f : 10.0f);
+}
+
+// sum_e offset_weight(e) (lo_e + hi_e) over a 16-element block held as its
+// elements 0..7 (lo) and 8..15 (hi), in the natural order.
+__device__ __forceinline__ float offset_sum16(const uint4& lo, const uint4& hi) {
+    const uint32_t a[4] = {lo.x, lo.y, lo.z, lo.w};
+    const uint32_t b[4] = {hi.x, hi.y, hi.z, hi.w};
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&a[j]));
+        const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&b[j]));
+        s = __fmaf_rn(offset_weight(2 * j), fa.x + fb.x, s);
+        s = __fmaf_rn(offset_weight(2 * j + 1), fa.y + fb.y, s);
+    }
+    return s;
+}
+
 // Xp[i, :] = x[perm[i] / topk, :] for the valid rows i < offsets[E]
-// (optionally in the interleaved 16-k order).
+// (optionally in the interleaved 16-k order); with csum (interleaved order
+// only) also csum[g * R + i] = sum over the 128-element group g of
+// offset_weight(k) x[k].
 __global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
-                              const int* __restrict__ offsets_end, int topk, int vec_per_row, int interleave,
-                              uint4* __restrict__ xp) {
+                              const int* __restrict__ offsets_end, int R, int topk, int vec_per_row, int interleave,
+                              uint4* __restrict__ xp, float* __restrict__ csum) {
     pdl_wait();
     pdl_trigger();
     const int i = blockIdx.x;
@@ -184,11 +211,25 @@ __global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict
     if (!interleave) {
         for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
     } else {
-        for (int v = 2 * threadIdx.x; v < vec_per_row; v += 2 * blockDim.x) {
-            uint4 a, b;
-            interleave_block(__ldg(src + v), __ldg(src + v + 1), a, b);
-            dst[v] = a;
-            dst[v + 1] = b;
+        // every warp runs the same number of rounds (the shuffles need all
+        // lanes); 8 consecutive threads hold one group's 16 vectors
+        for (int base = 0; base < vec_per_row; base += 2 * blockDim.x) {
+            const int v = base + 2 * threadIdx.x;
+            float part = 0.0f;
+            if (v < vec_per_row) {
+                const uint4 lo = __ldg(src + v), hi = __ldg(src + v + 1);
+                uint4 a, b;
+                interleave_block(lo, hi, a, b);
+                dst[v] = a;
+                dst[v + 1] = b;
+                if (csum) part = offset_sum16(lo, hi);
+            }
+            if (csum) {
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                part += __shfl_xor_sync(0xffffffffu, part, 4);
+                if ((threadIdx.x & 7) == 0 && v < vec_per_row) csum[static_cast<int64_t>(v >> 4) * R + i] = part;
+            }
         }
     }
 }
@@ -247,9 +288,13 @@ __device__ __forceinline__ float swiglu_clamped(float g, float u, float L) {
 // Split-K epilogue of w13: blockIdx.x = permuted row (valid rows only), each
 // thread 4 consecutive n; all KS partial loads of a thread are issued before
 // the first is used, and the splits are added in ascending order.
+// With csum, each warp (128 consecutive n = one group of w2's reduction) also
+// writes csum[g * R + r] = sum_n offset_weight(n) bf16(h[r, n]) for w2's
+// offset codes.
 template <int KS>
 __global__ void finalize_w13_kernel(const float* __restrict__ partial, int R, const int* __restrict__ offsets_end,
-                                    int N, float L, int interleave, __nv_bfloat16* __restrict__ h) {
+                                    int N, float L, int interleave, __nv_bfloat16* __restrict__ h,
+                                    float* __restrict__ csum) {
     pdl_wait();
     pdl_trigger();
     const int r = blockIdx.x;
@@ -272,6 +317,7 @@ __global__ void finalize_w13_kernel(const float* __restrict__ partial, int R, co
         us[0] += u[s].x; us[1] += u[s].y; us[2] += u[s].z; us[3] += u[s].w;
     }
     __nv_bfloat16* hr = h + static_cast<int64_t>(r) * N;
+    float part = 0.0f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
         const int n = n0 + e;
@@ -280,7 +326,14 @@ __global__ void finalize_w13_kernel(const float* __restrict__ partial, int R, co
             const int b = n & 15;
             col = (n & ~15) | (b < 8 ? 2 * b : 2 * (b - 8) + 1);
         }
-        hr[col] = __float2bfloat16_rn(swiglu_clamped(gs[e], us[e], L));
+        const __nv_bfloat16 hv = __float2bfloat16_rn(swiglu_clamped(gs[e], us[e], L));
+        hr[col] = hv;
+        part = __fmaf_rn(offset_weight(n), __bfloat162float(hv), part);
+    }
+    if (csum) {   // N % 128 == 0: whole warps return above, so all 32 lanes are here
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) part += __shfl_xor_sync(0xffffffffu, part, d);
+        if ((threadIdx.x & 31) == 0) csum[static_cast<int64_t>(n0 >> 7) * R + r] = part;
     }
 }
 
@@ -394,12 +447,12 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, 
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
-                          int interleave, __nv_bfloat16* xp, cudaStream_t stream) {
+                          int interleave, __nv_bfloat16* xp, float* csum, cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
     const int vpr = K / 8;
     const int threads = vpr >= 256 ? 256 : 32;
     return launch_pdl(gather_kernel, dim3(R), dim3(threads), 0, stream, reinterpret_cast<const uint4*>(x), perm,
-                      offsets_end, topk, vpr, interleave, reinterpret_cast<uint4*>(xp));
+                      offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp), interleave ? csum : nullptr);
 }
 
 cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
@@ -423,17 +476,17 @@ cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const i
 }
 
 cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
-                                int interleave, __nv_bfloat16* h, cudaStream_t stream) {
+                                int interleave, __nv_bfloat16* h, float* csum, cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
     const int threads = 128;
     const dim3 grid(R, (N / 4 + threads - 1) / threads);
     switch (ksplit) {
         case 2: return launch_pdl(finalize_w13_kernel<2>, grid, dim3(threads), 0, stream, partial, R, offsets_end, N,
-                                  limit, interleave, h);
+                                  limit, interleave, h, csum);
         case 4: return launch_pdl(finalize_w13_kernel<4>, grid, dim3(threads), 0, stream, partial, R, offsets_end, N,
-                                  limit, interleave, h);
+                                  limit, interleave, h, csum);
         case 8: return launch_pdl(finalize_w13_kernel<8>, grid, dim3(threads), 0, stream, partial, R, offsets_end, N,
-                                  limit, interleave, h);
+                                  limit, interleave, h, csum);
         default: return cudaErrorInvalidValue;
     }
 }
