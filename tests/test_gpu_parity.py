@@ -133,6 +133,18 @@ def test_forward_matches_oracle(moe, oracle, name):
 
 @pytest.mark.parametrize("name", ["prefill_w2_zipf", "prefill_w4_g64"])
 def test_prefill_forward_sampled_tokens(moe, oracle, name):
+    _check_sampled_tokens(moe, oracle, name)
+
+
+def test_decode_batch_64_sampled_tokens(moe, oracle):
+    """64 decode tokens (512 slots over 256 experts, 16-token tiles, no split K
+    at these sizes): the group-accumulate mode with offset codes in w13 (token
+    corrections from the gather) and plain codes in w2 (h written by the w13
+    epilogue itself), at full hidden sizes."""
+    _check_sampled_tokens(moe, oracle, "decode_w2_T64")
+
+
+def _check_sampled_tokens(moe, oracle, name):
     w = synth.get(name)
     inp = _inputs(w)
     out, status = _gpu_fwd(moe, w, gu.to_dev(inp))
