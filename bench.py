@@ -170,17 +170,28 @@ class ClockSampler:
 # ------------------------------------------------------------------ CPU oracle timing
 
 def cpu_model() -> str:
-    """The host CPU's model name (or the architecture when /proc does not say)."""
+    """The host CPU's model name: /proc/cpuinfo, else lscpu (Arm hosts list no
+    model name in /proc), else the architecture with the CPU part number."""
+    import platform
+    part = ""
     try:
         with open("/proc/cpuinfo") as f:
             for line in f:
                 key = line.split(":", 1)[0].strip().lower()
                 if key in ("model name", "cpu model", "hardware"):
                     return line.split(":", 1)[1].strip()
+                if key == "cpu part" and not part:
+                    part = line.split(":", 1)[1].strip()
     except OSError:
         pass
-    import platform
-    return platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine() + (f" (CPU part {part})" if part else "")
 
 
 def time_oracle(w: synth.Workload, inp: dict, budget_s: float, min_runs: int = 1, max_tokens: int | None = None):
