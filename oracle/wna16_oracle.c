@@ -28,7 +28,7 @@
  *   6. w2       y = bf16_rne( W2 h )
  *   7. combine  out[t] = bf16_rne( sum_j  w[t][j] * y[t*topk + j] ), j ascending
  *
- * Readings of points the pages leave open (each is listed in the design doc):
+ * Readings of points the pages leave open:
  *   - in-word order: field j of a word holds element p*word + j at bits
  *     [b*j, b*j + b), least significant first;
  *   - stored field = code + 2^(b-1) (2-bit: code + 2, 4-bit: code + 8);
