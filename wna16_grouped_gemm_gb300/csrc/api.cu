@@ -10,7 +10,9 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "../../include/wna16_moe.h"
 #include "gemm.h"
@@ -173,6 +175,24 @@ int device_info(DevInfo& d) {
     if (dev < 64) cache[dev] = d;
     return WNA16_OK;
 }
+
+}  // namespace
+
+cudaError_t wna16::ensure_dynamic_smem(const void* fn, int bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static std::mutex mu;
+    static std::map<std::pair<const void*, int>, int> allowed;   // (kernel, device) -> bytes already allowed
+    std::lock_guard<std::mutex> lock(mu);
+    int& cur = allowed[{fn, dev}];
+    if (bytes <= cur) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) cur = bytes;
+    return e;
+}
+
+namespace {
 
 // ---------------------------------------------------------------- TMA descriptors
 

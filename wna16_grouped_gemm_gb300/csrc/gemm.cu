@@ -1020,12 +1020,8 @@ template <int BITS, bool W13, int DW, int GA>
 static cudaError_t launch_impl(const CUtensorMap& tm_w, const CUtensorMap& tm_b, const GemmParams& p, int grid,
                                int smem_bytes, cudaStream_t stream) {
     auto kern = grouped_gemm_kernel<BITS, W13, DW, GA>;
-    static int attr_bytes = 0;   // largest dynamic smem size already allowed for this kernel
-    if (smem_bytes > attr_bytes) {
-        cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-        if (err != cudaSuccess) return err;
-        attr_bytes = smem_bytes;
-    }
+    cudaError_t err = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem_bytes);
+    if (err != cudaSuccess) return err;
     return launch_pdl(kern, dim3(grid), dim3(Roles<DW>::kThreads), static_cast<size_t>(smem_bytes), stream, tm_w,
                       tm_b, p);
 }

@@ -57,6 +57,11 @@ cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, con
 // Record a host-side error message for wna16_moe_last_error (api.cu); returns `code`.
 int set_error(int code, const char* fmt, ...);
 
+// Allow kernel `fn` at least `bytes` of dynamic shared memory on the current
+// device (api.cu): the opt-in is a per-device function attribute, set once per
+// device and kernel (thread-safe).
+cudaError_t ensure_dynamic_smem(const void* fn, int bytes);
+
 // Routing / gather / combine / pack kernels (kernels.cu).
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
                          int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream);

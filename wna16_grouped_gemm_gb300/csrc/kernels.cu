@@ -434,13 +434,8 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t n_words, i
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm, int* inv,
                          int4* tiles, int* n_tiles, int* status, cudaStream_t stream) {
     const int smem = (kRouteWarps * E + 64) * static_cast<int>(sizeof(int));
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (kRouteWarps * 1024 + 64) * static_cast<int>(sizeof(int)));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_kernel), smem);
+    if (e != cudaSuccess) return e;
     route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, nt, counts, offsets, perm, inv, tiles, n_tiles,
                                                     status);
     return cudaGetLastError();
