@@ -113,7 +113,10 @@ def recorded_traffic(workload: str, kernel: str):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 200 ms while the timed region runs; summary()
+    keeps the samples taken inside the given wall-clock window when there
+    are any."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -147,24 +150,36 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
+    @staticmethod
+    def parse(lines):
+        """(wall-clock seconds, sm MHz, max sm MHz, set of active reasons) per sample."""
+        import datetime
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        out = []
+        for ln in lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                sm, mx = float(parts[1]), float(parts[2])
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None   # kept, but never counted as inside the timed window
+            out.append((ts, sm, mx, {n for n, v in zip(names, parts[5:9]) if v.lower() == "active"}))
+        return out
+
+    def summary(self, t0=None, t1=None):
+        samples = self.parse(self.lines)
+        inside = [s for s in samples if t0 is not None and s[0] is not None and t0 <= s[0] <= t1]
+        use = inside or samples
+        if not use:
             return None
-        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=max(mx), reasons=sorted(reasons), samples=len(sm))
+        reasons = set().union(*(s[3] for s in use))
+        return dict(sm_mhz=statistics.median(s[1] for s in use), sm_max_mhz=max(s[2] for s in use),
+                    reasons=sorted(reasons), samples=len(use), in_timed_region=len(inside))
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -222,7 +237,9 @@ def time_oracle(w: synth.Workload, inp: dict, budget_s: float, min_runs: int = 1
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for about 1.5 s of timed forwards, at least 200; "
+                         "the reference arm: 100)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="decode_w2")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -230,6 +247,14 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--oracle-seconds", type=float, default=12.0)
     return ap.parse_args()
+
+
+def resolve_steps(per_step_ms: float, target_s: float = 1.5, lo: int = 200, hi: int = 10000) -> int:
+    """Default number of timed steps: enough for about target_s of timed
+    forwards (so that the 200 ms clock samples fall inside the timed region),
+    at least lo, at most hi, rounded to a hundred."""
+    n = target_s * 1000.0 / max(per_step_ms, 1e-6)
+    return int(min(hi, max(lo, round(n / 100.0) * 100)))
 
 
 def max_over_ranks(values, dist, device="cpu"):
@@ -264,6 +289,8 @@ def run_reference(args, w, rank, world, dist):
         return
     import oracle
     oracle.build()
+    if args.steps is None:
+        args.steps = 100
     inp = synth.make_all(w, args.seed)
     total = 0.0
     for i in range(args.warmup + args.steps):
@@ -334,6 +361,16 @@ def main():
         flush.fill_(1)
         fwd()
     torch.cuda.synchronize()
+    if args.steps is None:
+        # time a few more forwards to size the timed region (same count on every rank)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            flush.fill_(1)
+            fwd()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        args.steps = int(max_over_ranks([resolve_steps(e0.elapsed_time(e1) / 20)], dist, dev)[0])
     if moe.read_status(ws) != moe.OK:
         raise SystemExit(f"device status {moe.read_status(ws)} after warm-up")
 
@@ -345,12 +382,14 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as clk:
+        wall0 = time.time()
         for i in range(args.steps):
             flush.fill_(i & 0xFF)
             starts[i].record(stream)
             fwd()
             ends[i].record(stream)
         torch.cuda.synchronize()
+        wall1 = time.time()
     launches_per_forward = moe.binding.launches_last_forward()
     if dist:
         dist.barrier()
@@ -433,7 +472,7 @@ def main():
             e2e=dict(value=tokens / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=h2d,
                      d2h_bytes_per_step=d2h, ms_per_step=e2e_ms),
             gpu_launches=launches_per_forward * args.steps * world,
-            clocks=clk.summary(),
+            clocks=clk.summary(wall0, wall1),
         )
         if not args.no_cpu_baseline:
             max_tok = None if w.T <= 16 else 8
