@@ -81,6 +81,21 @@ def test_workspace_size(lib):
     assert big >= R * (4096 + 2048 + 4096) * 2
 
 
+def test_workspace_holds_split_k_partials_and_corrections(lib):
+    """Decode W2 (T=4, top-8 over 256 experts): 16-token tiles, at most
+    min(R, E) + R/16 + 1 = 35 tiles, so 560 units per GEMM, split 4 ways; the
+    partial sums take splits x row tiles x R x 256 fp32 (2 MiB for either
+    GEMM) and the offset-code corrections R x (K + N) / 128 fp32, on top of
+    the permuted x, h and y."""
+    T, K, N, E, topk = 4, 4096, 2048, 256, 8
+    R = T * topk
+    partial = 4 * (N // 128) * R * 256 * 4
+    assert partial == 4 * (K // 256) * R * 256 * 4 == 2 << 20
+    corrections = R * (K + N) // 128 * 4
+    need = R * (K + N + K) * 2 + partial + corrections
+    assert lib.wna16_moe_workspace_size(T, K, N, E, topk, 2) >= need
+
+
 def test_pack_rejects_on_host(lib):
     assert lib.wna16_moe_pack(A16, 4, 64, 3, A16, None) == binding.ERR_UNSUPPORTED
     assert lib.wna16_moe_pack(A16, 4, 60, 2, A16, None) == binding.ERR_INVALID_ARG
