@@ -5,10 +5,15 @@ One step = one full forward (route -> gather -> w13 GEMM + SwiGLU -> w2 GEMM
 HBM.  L2 is flushed (a 512 MiB write) before every timed step, outside the
 timed region; each step is timed with CUDA events on the launching stream.
 
-Default workload: decode, 4 concurrent sequences one step (T=4), hidden 4096,
-intermediate 2048, 256 experts, top-8, W2A16 with group 128.
+By default one run measures every workload in turn: the headline is the
+largest single-GPU workload (prefill chunk of 8192 tokens, hidden 4096,
+intermediate 2048, 256 experts, top-8, W4A16 with w13 group 128 and w2
+group 64); decode W2 (T=4), decode W4 (T=4 and T=1) and the 2048-token
+Zipf-routed W2 prefill go under "per_workload", each with its own value,
+roofline, end-to-end figure and stage times.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workloads A,B,..|--workload NAME]
+                  [--impl ours|reference]
 
 Under torchrun (N > 1) every rank runs an independent replica on its own
 batch (weak scaling, no collective on the data path); the step time is the
@@ -81,9 +86,12 @@ def load_peaks():
             return None, None
         hbm, src = pick("hbm_gbs", "hbm_copy_gbs")
         bf16, _ = pick("bf16_tflops")
+        sus, _ = pick("bf16_tflops_sustained")
         if hbm and bf16:
-            return dict(hbm_gbs=hbm, bf16_tflops=bf16, source="measured (MEASURED_PEAKS.json)")
-    return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS, source="fallback")
+            return dict(hbm_gbs=hbm, bf16_tflops=bf16, bf16_tflops_sustained=sus,
+                        source="measured (MEASURED_PEAKS.json: hbm_gbs copy, bf16_tflops burst)")
+    return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS, bf16_tflops_sustained=None,
+                source="fallback (6800 GB/s, 1900 TFLOP/s)")
 
 
 def kernel_source_hash() -> str:
@@ -112,6 +120,21 @@ def recorded_traffic(workload: str, kernel: str):
 
 # ------------------------------------------------------------------ clocks
 
+def smi_device(local: int, visible: str | None = None) -> str:
+    """The `nvidia-smi -i` argument for this process's CUDA device `local`.
+    nvidia-smi ignores CUDA_VISIBLE_DEVICES and numbers GPUs physically, so
+    the visible list is mapped back: its entry `local` (a physical index, a
+    GPU UUID or a PCI bus id, all accepted by `-i`) names the device."""
+    if visible is None:
+        visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if visible is None or not visible.strip():
+        return str(local)
+    entries = [e.strip() for e in visible.split(",") if e.strip()]
+    if local < len(entries):
+        return entries[local]
+    return str(local)
+
+
 class ClockSampler:
     """nvidia-smi samples every 200 ms while the timed region runs; summary()
     keeps the samples taken inside the given wall-clock window when there
@@ -120,7 +143,7 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index):
         self.index = index
         self.proc = None
         self.lines = []
@@ -234,19 +257,31 @@ def time_oracle(w: synth.Workload, inp: dict, budget_s: float, min_runs: int = 1
 
 # ------------------------------------------------------------------ main
 
-def parse():
+HEADLINE = "prefill_w4_g64"
+DEFAULT_WORKLOADS = ("prefill_w4_g64", "decode_w2", "decode_w4", "decode_w4_T1", "prefill_w2_zipf")
+
+
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None,
-                    help="timed steps (default: enough for about 1.5 s of timed forwards, at least 200; "
-                         "the reference arm: 100)")
+                    help="timed steps per workload (default: enough for about 1.5 s of timed forwards, at least "
+                         "200; the reference arm: 20)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="decode_w2")
+    ap.add_argument("--workload", default=None,
+                    help="run this one workload only (it becomes the headline)")
+    ap.add_argument("--workloads", default=",".join(DEFAULT_WORKLOADS),
+                    help="comma-separated workloads; the first is the headline, the others go under per_workload")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-flush", action="store_true",
+                    help="no L2 flush buffer (only for ncu captures, which flush caches themselves)")
     ap.add_argument("--oracle-seconds", type=float, default=12.0)
-    return ap.parse_args()
+    args = ap.parse_args(argv)
+    names = [args.workload] if args.workload else [n.strip() for n in args.workloads.split(",") if n.strip()]
+    args.workload_list = [synth.get(n) for n in names]
+    return args
 
 
 def resolve_steps(per_step_ms: float, target_s: float = 1.5, lo: int = 200, hi: int = 10000) -> int:
@@ -290,7 +325,7 @@ def run_reference(args, w, rank, world, dist):
     import oracle
     oracle.build()
     if args.steps is None:
-        args.steps = 100
+        args.steps = 20
     inp = synth.make_all(w, args.seed)
     total = 0.0
     for i in range(args.warmup + args.steps):
@@ -322,25 +357,29 @@ def workload_config(w):
                 l2="flushed before every timed step (512 MiB write)", weights="resident in HBM")
 
 
-def main():
-    args = parse()
-    w = synth.get(args.workload)
-    rank, world, local, dist = dist_setup(args.gpus)
-    if args.impl == "reference":
-        return run_reference(args, w, rank, world, dist)
+class WeightCache:
+    """Host weights per (shape, bits, groups, scales, seed): workloads that
+    share them (decode and prefill of one format) draw them once."""
 
+    def __init__(self):
+        self.key = None
+        self.val = None
+
+    def get(self, w: synth.Workload, seed: int):
+        key = (w.K, w.N, w.E, w.bits, w.g13, w.g2, w.scale_lo, w.scale_hi, seed)
+        if key != self.key:
+            self.val = None
+            self.key, self.val = key, synth.make_weights(w, seed)
+        return self.val
+
+
+def measure(w, inp, args, dev, dist, rank, world):
+    """Time one workload: the device-resident forward (the headline value),
+    the same steps with per-stage events (roofline), and the end-to-end
+    forward with host buffers.  Returns the per-workload record (rank 0) or None."""
     import torch
     import wna16_grouped_gemm_gb300 as moe
-    from wna16_grouped_gemm_gb300 import build
-    torch.cuda.set_device(local)
-    if rank == 0 or world == 1:
-        build.build()
-    if dist:
-        dist.barrier()
-    dev = torch.device("cuda", local)
-    inp = synth.make_all(w, args.seed + rank)
     facts = algorithmic(w, inp["ids"])
-
     x = torch.from_numpy(inp["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     ids = torch.from_numpy(inp["ids"]).to(dev)
     wts = torch.from_numpy(inp["weights"]).to(dev)
@@ -350,41 +389,46 @@ def main():
     w2s = torch.from_numpy(inp["w2_scales"]).to(dev)
     ws = moe.alloc_workspace(w.T, w.K, w.N, w.E, w.topk, w.bits, dev)
     out = torch.empty(w.T, w.K, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = None if args.no_flush else torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+
+    def do_flush(i):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
 
     def fwd(xx=x, ii=ids, ww=wts, oo=out):
         moe.forward(xx, ii, ww, w13p, w13s, w2p, w2s, bits=w.bits, group_size=w.g13, group_size_w2=w.g2,
                     swiglu_limit=w.swiglu_limit, out=oo, workspace=ws)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
+    for i in range(args.warmup):
+        do_flush(i)
         fwd()
     torch.cuda.synchronize()
-    if args.steps is None:
+    steps = args.steps
+    if steps is None:
         # time a few more forwards to size the timed region (same count on every rank)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for _ in range(20):
-            flush.fill_(1)
+        for i in range(20):
+            do_flush(i)
             fwd()
         e1.record(stream)
         torch.cuda.synchronize()
-        args.steps = int(max_over_ranks([resolve_steps(e0.elapsed_time(e1) / 20)], dist, dev)[0])
+        steps = int(max_over_ranks([resolve_steps(e0.elapsed_time(e1) / 20)], dist, dev)[0])
     if moe.read_status(ws) != moe.OK:
-        raise SystemExit(f"device status {moe.read_status(ws)} after warm-up")
+        raise SystemExit(f"{w.name}: device status {moe.read_status(ws)} after warm-up")
 
     # ---- device-resident timed region (the headline): forwards with nothing
     # else on the stream between their kernels, so they chain as in use
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ else local) as clk:
+    with ClockSampler(smi_device(torch.cuda.current_device())) as clk:
         wall0 = time.time()
-        for i in range(args.steps):
-            flush.fill_(i & 0xFF)
+        for i in range(steps):
+            do_flush(i)
             starts[i].record(stream)
             fwd()
             ends[i].record(stream)
@@ -397,20 +441,20 @@ def main():
     ms = sum(step_ms) / len(step_ms)
     status = moe.read_status(ws)
     if status != moe.OK:
-        raise SystemExit(f"device status {status} in timed region")
+        raise SystemExit(f"{w.name}: device status {status} in timed region")
 
     # ---- the same steps again with CUDA events between the stages, for the
     # per-kernel durations of the roofline (events between kernels cost a
     # little and stop consecutive kernels from overlapping their launch, so
     # these stage times are upper bounds of the kernels' own durations)
     stage_ms = {k: [] for k in moe.binding.STAGES}
-    moe.profile(args.steps)
+    moe.profile(steps)
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+    for i in range(steps):
+        do_flush(i)
         fwd()
     torch.cuda.synchronize()
-    for rec in moe.profile_read(args.steps):
+    for rec in moe.profile_read(steps):
         for k, v in rec.items():
             stage_ms[k].append(v)
     moe.profile(0)
@@ -421,10 +465,10 @@ def main():
     wts_h = torch.from_numpy(inp["weights"]).pin_memory()
     out_h = torch.empty(w.T, w.K, dtype=torch.bfloat16).pin_memory()
     xd, idd, wd = torch.empty_like(x), torch.empty_like(ids), torch.empty_like(wts)
-    e_st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    e_en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+    e_st = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    e_en = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        do_flush(i)
         e_st[i].record(stream)
         xd.copy_(x_h, non_blocking=True)
         idd.copy_(ids_h, non_blocking=True)
@@ -433,52 +477,103 @@ def main():
         out_h.copy_(out, non_blocking=True)
         e_en[i].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_st, e_en)) / args.steps
+    e2e_ms = sum(s.elapsed_time(e) for s, e in zip(e_st, e_en)) / steps
     h2d = x_h.numel() * 2 + ids_h.numel() * 4 + wts_h.numel() * 4
     d2h = out_h.numel() * 2
 
-    # ---- max over ranks
-    ms, e2e_ms = max_over_ranks([ms, e2e_ms], dist, dev)
+    st_local = [(sum(v) / len(v) if v else 0.0) for v in stage_ms.values()]
+    red = max_over_ranks([ms, e2e_ms] + st_local, dist, dev)
+    ms, e2e_ms = red[0], red[1]
+    st = dict(zip(stage_ms.keys(), red[2:]))
+    del x, ids, wts, w13p, w13s, w2p, w2s, ws, out, flush, xd, idd, wd
+    if rank != 0:
+        return None
+
+    peaks = load_peaks()
+    decode = is_decode(w)
+    dom = "w13" if st["w13"] >= st["w2"] else "w2"
+    dom_ms = st[dom]
+    if decode:
+        achieved = facts[f"{dom}_kernel_bytes"] / (dom_ms * 1e-3) / 1e9
+        roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
+                    frac=achieved / peaks["hbm_gbs"])
+    else:
+        achieved = facts[f"{dom}_flops"] / (dom_ms * 1e-3) / 1e12
+        roof = dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                    frac=achieved / peaks["bf16_tflops"])
+        if peaks.get("bf16_tflops_sustained"):
+            roof["frac_vs_sustained_peak"] = achieved / peaks["bf16_tflops_sustained"]
+    roof.update(kernel=f"grouped_gemm_{dom}", peak_source=peaks["source"],
+                algorithmic_per_launch=facts[f"{dom}_kernel_bytes"] if decode else facts[f"{dom}_flops"],
+                algorithmic_unit="bytes" if decode else "flop", traffic=recorded_traffic(w.name, dom),
+                traffic_unit="DRAM bytes per launch")
+    tokens = w.T * world
+    return dict(
+        value=tokens / (ms * 1e-3), unit="tokens/s", steps=steps, ms_per_step=ms, config=workload_config(w),
+        roofline=roof,
+        forward=dict(hbm_gbs=facts["forward_bytes"] / (ms * 1e-3) / 1e9,
+                     hbm_frac=facts["forward_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                     tflops=facts["forward_flops"] / (ms * 1e-3) / 1e12,
+                     tensor_frac=facts["forward_flops"] / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                     algorithmic_bytes=facts["forward_bytes"], algorithmic_flops=facts["forward_flops"],
+                     active_experts=facts["active_experts"], stage_ms=st,
+                     step_ms_median=statistics.median(step_ms)),
+        e2e=dict(value=tokens / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=h2d, d2h_bytes_per_step=d2h,
+                 ms_per_step=e2e_ms),
+        gpu_launches=launches_per_forward * steps * world,
+        clocks=clk.summary(wall0, wall1),
+    )
+
+
+def main(argv=None):
+    args = parse(argv)
+    wl = args.workload_list
+    rank, world, local, dist = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, wl[0], rank, world, dist)
+
+    import torch
+    import wna16_grouped_gemm_gb300 as moe
+    from wna16_grouped_gemm_gb300 import build
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        build.build()
+    if dist:
+        dist.barrier()
+    moe.load_library()
+    dev = torch.device("cuda", local)
+    cache = WeightCache()
+    records = {}
+    head_inp = None
+    for w in wl:
+        w13p, w13s, w2p, w2s = cache.get(w, args.seed + rank)
+        ids, wts = synth.make_routing(w, args.seed + rank)
+        inp = dict(x=synth.make_x(w, args.seed + rank), ids=ids, weights=wts, w13_packed=w13p, w13_scales=w13s,
+                   w2_packed=w2p, w2_scales=w2s)
+        records[w.name] = measure(w, inp, args, dev, dist, rank, world)
+        if w is wl[0]:
+            head_inp = inp
+        torch.cuda.empty_cache()
 
     if rank == 0:
-        peaks = load_peaks()
-        st = {k: (sum(v) / len(v) if v else 0.0) for k, v in stage_ms.items()}
-        decode = is_decode(w)
-        dom = "w13" if st["w13"] >= st["w2"] else "w2"
-        dom_ms = st[dom]
-        if decode:
-            achieved = facts[f"{dom}_kernel_bytes"] / (dom_ms * 1e-3) / 1e9
-            roof = dict(bound="hbm", achieved=achieved, peak=peaks["hbm_gbs"], unit="GB/s",
-                        frac=achieved / peaks["hbm_gbs"])
-        else:
-            achieved = facts[f"{dom}_flops"] / (dom_ms * 1e-3) / 1e12
-            roof = dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
-                        frac=achieved / peaks["bf16_tflops"])
-        roof.update(kernel=f"grouped_gemm_{dom}", peak_source=peaks["source"],
-                    algorithmic_per_launch=facts[f"{dom}_kernel_bytes"] if decode else facts[f"{dom}_flops"],
-                    traffic=recorded_traffic(w.name, dom))
-        tokens = w.T * world
+        head = wl[0]
+        r = records[head.name]
         line = dict(
             metric="routed-MoE tokens/s (W2/W4A16 WNA16 forward)",
-            value=tokens / (ms * 1e-3), unit="tokens/s", n_gpus=world, steps=args.steps, warmup=args.warmup,
-            ms_per_step=ms, higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
-            data="synthetic", config=workload_config(w), roofline=roof,
-            forward=dict(hbm_gbs=facts["forward_bytes"] / (ms * 1e-3) / 1e9,
-                         hbm_frac=facts["forward_bytes"] / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                         tflops=facts["forward_flops"] / (ms * 1e-3) / 1e12,
-                         tensor_frac=facts["forward_flops"] / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-                         algorithmic_bytes=facts["forward_bytes"], active_experts=facts["active_experts"],
-                         stage_ms=st, step_ms_median=statistics.median(step_ms)),
-            e2e=dict(value=tokens / (e2e_ms * 1e-3), unit="tokens/s", h2d_bytes_per_step=h2d,
-                     d2h_bytes_per_step=d2h, ms_per_step=e2e_ms),
-            gpu_launches=launches_per_forward * args.steps * world,
-            clocks=clk.summary(wall0, wall1),
+            value=r["value"], unit="tokens/s", n_gpus=world, steps=r["steps"], warmup=args.warmup,
+            ms_per_step=r["ms_per_step"], higher_is_better=True, scaling="weak", vs_baseline=None, dtype="bf16",
+            data="synthetic (seeded; no dataset or checkpoint)", config=r["config"], roofline=r["roofline"],
+            forward=r["forward"], e2e=r["e2e"], gpu_launches=r["gpu_launches"], clocks=r["clocks"],
         )
+        if len(wl) > 1:
+            line["per_workload"] = {w.name: records[w.name] for w in wl[1:]}
         if not args.no_cpu_baseline:
-            max_tok = None if w.T <= 16 else 8
-            rate, sample, cores, _ = time_oracle(w, inp, args.oracle_seconds, 1, max_tok)
+            # the headline workload's own inputs (the host arrays are still held)
+            inp = head_inp
+            max_tok = None if head.T <= 16 else 8
+            rate, sample, cores, _ = time_oracle(head, inp, args.oracle_seconds, 1, max_tok)
             line["cpu_baseline"] = dict(value=rate, unit="tokens/s", cores=cores, kind="oracle", sample=sample,
-                                        cpu=cpu_model())
+                                        cpu=cpu_model(), workload=head.name)
         print(json.dumps(line))
     if dist:
         dist.destroy_process_group()

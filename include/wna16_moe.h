@@ -162,15 +162,20 @@ WNA16_API int wna16_moe_combine(const void* y, const float* topk_weights, int64_
  * (wna16_moe_workspace_size) exceeds 32 MiB are rejected with
  * WNA16_ERR_WORKSPACE_TOO_SMALL and a message, and nothing is launched
  * (decode batches up to about 160 tokens of hidden 4096 / intermediate 2048 /
- * 256 experts / top-8 fit).  The call allocates nothing: no cudaMalloc or
- * cudaFree and no allocating library routine.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Every
- * call uses the same array and it keeps the previous call's contents (the
- * forward clears what must start at zero); calls that overlap on the GPU --
- * on different streams or from different host threads -- race on it, so the
- * caller must serialise them.  The device status word lives in that shared
- * array and cannot be read back by the caller. */
+ * 256 experts / top-8 fit).  The call itself allocates nothing: no cudaMalloc
+ * or cudaFree and no allocating library routine.  The first call on a device
+ * (and the first after that device's context changes) looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; under
+ * lazy module loading that lookup is also when the driver loads the array's
+ * module and reserves its 32 MiB, so the first call can fail with
+ * WNA16_ERR_CUDA when the device is out of memory.  Make one call (or any
+ * call that succeeds) at start-up, while memory is free and before any
+ * stream capture; later calls reuse the address.  Every call uses the same
+ * array and it keeps the previous call's contents (the forward clears what
+ * must start at zero); calls that overlap on the GPU -- on different streams
+ * or from different host threads -- race on it, so the caller must serialise
+ * them.  The device status word lives in that shared array and cannot be read
+ * back by the caller. */
 WNA16_API int wna16_moe_forward_noalloc(const void* x, const int32_t* topk_ids, const float* topk_weights,
                                         const int32_t* w13_packed, const uint16_t* w13_scales,
                                         const int32_t* w2_packed, const uint16_t* w2_scales,

@@ -73,7 +73,7 @@ def _load():
     lib.oracle_route.argtypes = [P, I64, I64, P, P, P, P]
     lib.oracle_route.restype = I
     lib.oracle_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I64, I64, I,
-                                   ctypes.c_float, I, P, I64, P, P, P]
+                                   ctypes.c_float, I, P, I64, P, P, P, P]
     lib.oracle_forward.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
@@ -165,10 +165,12 @@ def forward(x_bf16: np.ndarray, ids: np.ndarray, weights: np.ndarray,
             w2_packed: np.ndarray, w2_scales: np.ndarray,
             *, bits: int, group_size: int, group_size_w2: int | None = None,
             swiglu_limit: float = 7.0, accum: str = "fp64", tokens=None,
-            return_intermediates: bool = False):
+            return_intermediates: bool = False, h_in: np.ndarray | None = None):
     """Oracle forward.  ``x_bf16`` is uint16 [T, K] (BF16 bit patterns);
     returns BF16 bit patterns ``out`` [n_tok, K] (and h [n_tok*topk, N],
-    y [n_tok*topk, K] in slot order when ``return_intermediates``)."""
+    y [n_tok*topk, K] in slot order when ``return_intermediates``).
+    With ``h_in`` (BF16 bits [n_tok*topk, N], slot order) the gate/up
+    projection and SwiGLU are skipped and ``h_in`` is used as h."""
     x = _c(x_bf16, np.uint16)
     ids = _c(ids, np.int32)
     wts = _c(weights, np.float32)
@@ -186,10 +188,15 @@ def forward(x_bf16: np.ndarray, ids: np.ndarray, weights: np.ndarray,
     out = np.empty((n_tok, K), np.uint16)
     h = np.empty((n_tok * topk, N), np.uint16) if return_intermediates else None
     y = np.empty((n_tok * topk, K), np.uint16) if return_intermediates else None
+    hin = None
+    if h_in is not None:
+        hin = _c(h_in, np.uint16)
+        if hin.shape != (n_tok * topk, N):
+            raise OracleError(f"h_in must be [{n_tok * topk}, {N}]")
     rc = _load().oracle_forward(
         _ptr(x), _ptr(ids), _ptr(wts), _ptr(w13p), _ptr(w13s), _ptr(w2p), _ptr(w2s),
         T, K, N, E, topk, group_size, g2, bits, float(swiglu_limit),
-        0 if accum == "fp64" else 1, _ptr(tok), n_tok, _ptr(out), _ptr(h), _ptr(y))
+        0 if accum == "fp64" else 1, _ptr(tok), n_tok, _ptr(hin), _ptr(out), _ptr(h), _ptr(y))
     if rc != 0:
         raise OracleError("forward: bad arguments or expert id out of range")
     if return_intermediates:

@@ -301,6 +301,9 @@ static float swiglu_f(float g, float u, float L)
  * w2s      fp16  [E, K, N/g2]
  * accum    0: fp64 dot products and combine; 1: fp32 (ascending order)
  * tokens   optional list of n_tok token indices to evaluate (NULL: all T)
+ * h_in     optional bf16 [n_tok*topk, N] (slot order): when given, steps 4 and 5
+ *          are skipped and these values are h (to run steps 6 and 7 on an h
+ *          computed elsewhere)
  * out      bf16 [n_tok, K]
  * h_out    optional bf16 [n_tok*topk, N]  (slot order t*topk + j)
  * y_out    optional bf16 [n_tok*topk, K]
@@ -311,7 +314,7 @@ int oracle_forward(const uint16_t* x, const int32_t* ids, const float* wts,
                    const int32_t* w2p, const uint16_t* w2s,
                    int64_t T, int64_t K, int64_t N, int64_t E, int topk,
                    int64_t g13, int64_t g2, int bits, float swiglu_limit, int accum,
-                   const int64_t* tokens, int64_t n_tok,
+                   const int64_t* tokens, int64_t n_tok, const uint16_t* h_in,
                    uint16_t* out, uint16_t* h_out, uint16_t* y_out)
 {
     if (bits != 2 && bits != 4) return -1;
@@ -355,7 +358,7 @@ int oracle_forward(const uint16_t* x, const int32_t* ids, const float* wts,
 
         /* step 2 for this expert */
         #pragma omp parallel for schedule(static)
-        for (int64_t r = 0; r < 2 * N; ++r)
+        for (int64_t r = 0; r < (h_in ? 0 : 2 * N); ++r)
             dequant_row(w13p + (e * 2 * N + r) * (K / p), w13s + (e * 2 * N + r) * (K / g13),
                         K, g13, bits, W13 + r * K);
         #pragma omp parallel for schedule(static)
@@ -374,6 +377,10 @@ int oracle_forward(const uint16_t* x, const int32_t* ids, const float* wts,
             /* steps 4 and 5: h = swiglu(W1 x, W3 x), rounded to bf16 */
             #pragma omp parallel for schedule(static)
             for (int64_t n = 0; n < N; ++n) {
+                if (h_in) {
+                    hbuf[s * N + n] = oracle_bf16_to_double(h_in[s * N + n]);
+                    continue;
+                }
                 const double* w1 = W13 + (gate0 + n) * K;
                 const double* w3 = W13 + (up0 + n) * K;
                 if (accum == 0) {

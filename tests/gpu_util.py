@@ -4,7 +4,7 @@ path (routing indices and packed words: bit-exact; BF16 tensors: relative
 L2 <= 1e-3, and max-abs <= 2e-2 where the BF16 spacing of the reference
 value is finer than that -- an element whose reference has a BF16 ulp above
 2e-2 (|ref| >= 4) may differ by that one ulp, the smallest difference BF16
-can express there)."""
+can express there; at most 0.1 % of the elements may need that allowance)."""
 from __future__ import annotations
 
 import numpy as np
@@ -55,10 +55,16 @@ def compare_bf16(got_bits, ref_bits, what: str = "") -> dict:
     allowed = np.maximum(MAX_ABS, ulp_ref)
     stats = dict(what=what, n=int(g.size), max_abs=float(d.max()) if d.size else 0.0, rel_l2=rel,
                  max_abs_excess=float((d - allowed).max()) if d.size else 0.0,
+                 # elements inside the bar only through the one-ulp allowance for |ref| >= 4
+                 widened=int((d > MAX_ABS).sum()),
                  exact=float((ulp == 0).mean()) if ulp.size else 1.0,
                  le1ulp=float((ulp <= 1).mean()) if ulp.size else 1.0,
                  nonfinite=int((~np.isfinite(g)).sum()))
     return stats
+
+
+# At most this fraction of the elements may rely on the one-ulp allowance.
+MAX_WIDENED_FRAC = 1e-3
 
 
 def assert_close(got_bits, ref_bits, what: str = "", max_abs=MAX_ABS, rel_l2=REL_L2) -> dict:
@@ -68,6 +74,7 @@ def assert_close(got_bits, ref_bits, what: str = "", max_abs=MAX_ABS, rel_l2=REL
     assert s["rel_l2"] <= rel_l2, s
     if max_abs == MAX_ABS:
         assert s["max_abs_excess"] <= 0.0, s
+        assert s["widened"] <= MAX_WIDENED_FRAC * s["n"], s
     else:
         assert s["max_abs"] <= max_abs, s
     return s

@@ -74,11 +74,16 @@ def py_dequant_matrix(packed, scales_bits, K, group, bits):
 
 
 def brute_force_forward(x_bits, ids, wts, w13p, w13s_bits, w2p, w2s_bits, K, N, E, topk,
-                        g13, g2, bits, limit):
-    """Plain loops over tokens, slots, rows and columns; fp64 sums in
-    ascending order; BF16 rounding of the weights, h, y and out."""
+                        g13, g2, bits, limit, fp32=False, h_in=None):
+    """Plain loops over tokens, slots, rows and columns; sums in ascending
+    order, in fp64 (default) or, with ``fp32``, in IEEE binary32 with every
+    product and every addition rounded (numpy float32 scalars; SiLU's
+    exponential in binary32 too); BF16 rounding of the weights, h, y and out.
+    With ``h_in`` (BF16 bits per slot t*topk + j, [T*topk, N]) the gate/up
+    projection and SwiGLU are skipped and h_in is used as h."""
+    f32 = np.float32
     T = len(x_bits)
-    W13 = [py_dequant_matrix(w13p[e], w13s_bits[e], K, g13, bits) for e in range(E)]
+    W13 = None if h_in is not None else [py_dequant_matrix(w13p[e], w13s_bits[e], K, g13, bits) for e in range(E)]
     W2 = [py_dequant_matrix(w2p[e], w2s_bits[e], N, g2, bits) for e in range(E)]
     out = []
     for t in range(T):
@@ -88,28 +93,53 @@ def brute_force_forward(x_bits, ids, wts, w13p, w13s_bits, w2p, w2s_bits, K, N, 
             e = int(ids[t][j])
             h = []
             for n in range(N):
-                g = 0.0
-                u = 0.0
-                for k in range(K):
-                    g += W13[e][n][k] * xs[k]
-                for k in range(K):
-                    u += W13[e][N + n][k] * xs[k]
-                gc = min(g, limit)
-                uc = max(-limit, min(u, limit))
-                val = gc / (1.0 + math.exp(-gc)) * uc
+                if h_in is not None:
+                    h.append(bf16_value(int(h_in[t * topk + j][n])))
+                    continue
+                if fp32:
+                    g = f32(0.0)
+                    u = f32(0.0)
+                    for k in range(K):
+                        g = f32(g + f32(f32(W13[e][n][k]) * f32(xs[k])))
+                        u = f32(u + f32(f32(W13[e][N + n][k]) * f32(xs[k])))
+                    gc = min(g, f32(limit))
+                    uc = max(f32(-limit), min(u, f32(limit)))
+                    val = float(f32(f32(gc / f32(f32(1.0) + np.exp(f32(-gc)))) * uc))
+                else:
+                    g = 0.0
+                    u = 0.0
+                    for k in range(K):
+                        g += W13[e][n][k] * xs[k]
+                    for k in range(K):
+                        u += W13[e][N + n][k] * xs[k]
+                    gc = min(g, limit)
+                    uc = max(-limit, min(u, limit))
+                    val = gc / (1.0 + math.exp(-gc)) * uc
                 h.append(bf16_value(bf16_bits_exact(val)))
             y = []
             for m in range(K):
-                acc = 0.0
-                for n in range(N):
-                    acc += W2[e][m][n] * h[n]
+                if fp32:
+                    acc = f32(0.0)
+                    for n in range(N):
+                        acc = f32(acc + f32(f32(W2[e][m][n]) * f32(h[n])))
+                    acc = float(acc)
+                else:
+                    acc = 0.0
+                    for n in range(N):
+                        acc += W2[e][m][n] * h[n]
                 y.append(bf16_value(bf16_bits_exact(acc)))
             ys.append(y)
         row = []
         for m in range(K):
-            acc = 0.0
-            for j in range(topk):
-                acc += float(np.float32(wts[t][j])) * ys[j][m]
+            if fp32:
+                acc = f32(0.0)
+                for j in range(topk):
+                    acc = f32(acc + f32(f32(wts[t][j]) * f32(ys[j][m])))
+                acc = float(acc)
+            else:
+                acc = 0.0
+                for j in range(topk):
+                    acc += float(np.float32(wts[t][j])) * ys[j][m]
             row.append(bf16_bits_exact(acc))
         out.append(row)
     return np.array(out, dtype=np.uint16)

@@ -59,3 +59,15 @@ def test_clock_summary_keeps_the_timed_window():
     odd.lines = ["Tue Jan  1 12:00:00 2026, 2070, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
     s3 = odd.summary(t0, t1)
     assert s3["samples"] == 1 and s3["in_timed_region"] == 0 and s3["sm_mhz"] == 2070
+
+
+def test_clock_sampler_names_the_physical_gpu():
+    """nvidia-smi numbers GPUs physically: device 0 of a process that sees
+    CUDA_VISIBLE_DEVICES=5,2 is physical GPU 5, and a UUID list maps to the
+    UUID."""
+    b = _bench()
+    assert b.smi_device(0, "5,2") == "5"
+    assert b.smi_device(1, "5, 2") == "2"
+    assert b.smi_device(0, "GPU-1234abcd-0000-1111-2222-333344445555") == "GPU-1234abcd-0000-1111-2222-333344445555"
+    assert b.smi_device(3, None if False else "") == "3"
+    assert b.smi_device(1, "7") == "1"          # more devices than listed: leave the index alone

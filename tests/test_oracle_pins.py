@@ -162,6 +162,37 @@ def pin_brute_force(oracle):
         assert np.array_equal(got, ref), bits
 
 
+def pin_fp32_mode(oracle):
+    """The fp32 accumulation mode equals the same loops written with numpy
+    binary32 scalars (every product and sum rounded).  SiLU's exponential
+    comes from two different binary32 implementations (libm and numpy), so a
+    rare one-ulp difference of h is allowed to show through."""
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=2, K=32, N=16, E=3, topk=2, g13=8, g2=8)
+        got = _run(oracle, c, accum="fp32")
+        ref = ind.brute_force_forward(
+            c["x"], c["ids"], c["weights"], c["w13_packed"], c["w13_scales"].view(np.uint16),
+            c["w2_packed"], c["w2_scales"].view(np.uint16), c["K"], c["N"], c["E"], c["topk"],
+            c["g13"], c["g2"], bits, 7.0, fp32=True)
+        diff = np.abs(got.astype(np.int32) - ref.astype(np.int32))
+        assert diff.max() <= 1 and (diff == 0).mean() >= 0.95, (bits, diff.max(), (diff == 0).mean())
+
+
+def pin_given_h(oracle):
+    """With h given, the oracle runs the down projection and the combine only:
+    the pure-Python loops fed the same h give the same bits."""
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=2, K=32, N=16, E=3, topk=2, g13=8, g2=8)
+        rng = np.random.default_rng(17)
+        h = synth.to_bf16_bits(rng.standard_normal((2 * 2, 16), dtype=np.float32))
+        got = _run(oracle, c, h_in=h)
+        ref = ind.brute_force_forward(
+            c["x"], c["ids"], c["weights"], c["w13_packed"], c["w13_scales"].view(np.uint16),
+            c["w2_packed"], c["w2_scales"].view(np.uint16), c["K"], c["N"], c["E"], c["topk"],
+            c["g13"], c["g2"], bits, 7.0, h_in=h)
+        assert np.array_equal(got, ref), bits
+
+
 def _dense_mlp_torch(c, limit):
     """One expert, top-1, weight 1: a plain dense SwiGLU MLP in torch fp64 on the
     dequantised weights (numpy unpacking, torch bf16 rounding)."""
@@ -292,7 +323,8 @@ def pin_split_routing_weight(oracle):
 
 PINS = [pin_fp16_decode, pin_bf16_rounding, pin_hand_words, pin_pack_roundtrip, pin_dequant,
         pin_route, pin_zero_codes, pin_brute_force, pin_dense_mlp, pin_clamp_closed_form,
-        pin_scale_doubling, pin_relabel_and_token_permutation, pin_split_routing_weight]
+        pin_scale_doubling, pin_relabel_and_token_permutation, pin_split_routing_weight, pin_fp32_mode,
+        pin_given_h]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

@@ -5,9 +5,10 @@ device memory is all owned by another allocator, or their latency-critical
 path must not risk an allocation failing or synchronising the device);
 `wna16_moe_forward_noalloc` serves them with its scratch in a static device
 array inside the library.  This test checks that two calls in a row -- the
-second one finding the first one's data still in that array -- each match
-the regular workspace entry point within the parity tolerance, and that a
-size too large for the array is refused on the host.
+second one finding the first one's data still in that array -- each give
+the same bits as the regular workspace entry point (both run the same
+deterministic plan, so the outputs must be identical, well inside the parity
+tolerance), and that a size too large for the array is refused on the host.
 
 The file name sorts last so that a run stopping at its first failure has
 already run every other test; it also passes on its own in a fresh process.
@@ -55,7 +56,9 @@ def test_noalloc_forward_matches_workspace_forward_twice():
         rc = _noalloc(lib, d, w, out)
         assert rc == moe.OK, lib.wna16_moe_last_error().decode()
         torch.cuda.synchronize()
-        gu.assert_close(gu.host_bits(out), gu.host_bits(ref), f"noalloc {w.name}")
+        got, want = gu.host_bits(out), gu.host_bits(ref)
+        gu.assert_close(got, want, f"noalloc {w.name}")
+        assert np.array_equal(got, want), f"noalloc {w.name}: not bit-identical to the workspace forward"
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():

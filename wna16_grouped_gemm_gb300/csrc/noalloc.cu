@@ -7,6 +7,7 @@
 // the failure or the implicit device synchronisation an allocation can bring.
 // They still own and pass every input and output; only the scratch (routing
 // lists, permuted activations, h, y, split-K sums) moves into g_scratch below.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -26,10 +27,32 @@ __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 // Device address of g_scratch per device.  In host code `g_scratch` names a
 // host-side stand-in, not device memory, so the address must come from
-// cudaGetSymbolAddress, taken once per device with that device current.
+// cudaGetSymbolAddress, taken with that device current.  The address belongs
+// to the device's current context: it is cached together with that context
+// and looked up again when the context changes (after cudaDeviceReset, or a
+// primary-context reset, the old address is stale).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
+
 std::mutex g_mu;
 constexpr int kMaxDevices = 64;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+    CUcontext ctx = nullptr;
+    void* ptr = nullptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 
 int scratch_address(void** out) {
     int dev = 0;
@@ -37,15 +60,24 @@ int scratch_address(void** out) {
     if (e != cudaSuccess) return wna16::set_error(WNA16_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices)
         return wna16::set_error(WNA16_ERR_UNSUPPORTED, "device %d: at most %d devices", dev, kMaxDevices);
+    CtxGetCurrentFn get = ctx_get_current();
+    if (!get) return wna16::set_error(WNA16_ERR_CUDA, "cuCtxGetCurrent is not available from the driver");
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return wna16::set_error(WNA16_ERR_CUDA, "cuCtxGetCurrent failed");
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    ScratchAddr& a = g_scratch_addr[dev];
+    if (!a.ptr || !ctx || a.ctx != ctx) {
+        // (with no current context yet, the runtime makes the device's primary
+        // context current here)
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_scratch);
         if (e != cudaSuccess || !p)
             return wna16::set_error(WNA16_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-        g_scratch_ptr[dev] = p;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return wna16::set_error(WNA16_ERR_CUDA, "cuCtxGetCurrent failed");
+        a.ctx = ctx;
+        a.ptr = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = a.ptr;
     return WNA16_OK;
 }
 
