@@ -33,6 +33,9 @@ MUTATIONS = {
     "no_route_weight": 7,
     "unstable_perm": 8,
     "silu_sign": 9,
+    "topk_tie_high": 10,
+    "topk_no_renorm": 11,
+    "topk_no_bias": 12,
 }
 
 
@@ -75,6 +78,8 @@ def _load():
     lib.oracle_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I64, I64, I,
                                    ctypes.c_float, I, P, I64, P, P, P, P]
     lib.oracle_forward.restype = I
+    lib.oracle_route_topk.argtypes = [P, P, I64, I64, I, P, P]
+    lib.oracle_route_topk.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     _lib = lib
@@ -202,3 +207,19 @@ def forward(x_bf16: np.ndarray, ids: np.ndarray, weights: np.ndarray,
     if return_intermediates:
         return out, h, y
     return out
+
+
+def route_topk(logits: np.ndarray, k: int, bias: np.ndarray | None = None):
+    """Router: softmax of (logits + bias) over the experts, the top k (ties to
+    the lower expert index), renormalised.  logits fp32 [T, E], bias fp32 [E]
+    or None; returns (ids int32 [T, k], weights fp32 [T, k])."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    b = None if bias is None else _c(bias, np.float32)
+    if b is not None and b.shape != (E,):
+        raise OracleError("bias must be [E]")
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    if _load().oracle_route_topk(_ptr(lg), _ptr(b), T, E, k, _ptr(ids), _ptr(w)) != 0:
+        raise OracleError("route_topk: k must be in [1, E]")
+    return ids, w

@@ -64,7 +64,10 @@ enum {
     MUT_NO_ROUTE_WEIGHT = 7,/* drop the routing weight in the combine           */
     MUT_UNSTABLE_PERM = 8,  /* emit each expert's slots in descending order     */
     MUT_SILU_SIGN = 9,      /* silu(z) = z / (1 + exp(z))                        */
-    MUT_LAST = 10
+    MUT_TOPK_TIE_HIGH = 10, /* router: equal scores go to the higher index       */
+    MUT_TOPK_NO_RENORM = 11,/* router: weights left as full-softmax probabilities */
+    MUT_TOPK_NO_BIAS = 12,  /* router: the bias is ignored                       */
+    MUT_LAST = 13
 };
 static int g_mutation = MUT_NONE;
 
@@ -446,6 +449,83 @@ int oracle_forward(const uint16_t* x, const int32_t* ids, const float* wts,
         for (int64_t q = 0; q < R * K; ++q) y_out[q] = oracle_bf16_rne(ybuf[q]);
 
     free(W13); free(W2); free(hbuf); free(ybuf); free(xrow);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Router: softmax over the experts, top-k, renormalisation.             */
+/* ------------------------------------------------------------------ */
+
+/*
+ * The routing that produces topk_ids / topk_weights from router logits, in
+ * the order the workload description gives it ("top-k softmax routing from
+ * N(0,1) logits", renormalised; the popularity skew enters as a logit bias):
+ *
+ *   z_e   = fp32( logits[t][e] + bias[e] )             (bias optional)
+ *   p_e   = exp(z_e - max z) / sum_e' exp(z_e' - max z)  softmax, fp64
+ *   ids   = the k experts of largest p, in descending order; equal values
+ *           go to the lower expert index
+ *   w_j   = fp32( p_ids[j] / sum_i p_ids[i] )          renormalised, fp64
+ *
+ * Which experts are chosen is an integer decision taken on floating point,
+ * so it is taken on z itself, in the fp32 that both this definition and the
+ * kernel compute it in: exp is increasing and the softmax denominator is
+ * shared, so the order of p is the order of z (exactly so while the fp64
+ * exponentials do not underflow, i.e. while the logits span less than about
+ * 700).
+ *
+ * logits fp32 [T, E]; bias fp32 [E] or NULL; ids int32 [T, k]; weights fp32
+ * [T, k].  Returns 0, or -1 on a bad argument (k outside [1, E]).
+ */
+int oracle_route_topk(const float* logits, const float* bias, int64_t T, int64_t E, int k,
+                      int32_t* ids, float* weights)
+{
+    if (T < 0 || E <= 0 || k < 1 || k > E) return -1;
+    float* z = (float*)malloc(sizeof(float) * (size_t)E);
+    double* p = (double*)malloc(sizeof(double) * (size_t)E);
+    unsigned char* taken = (unsigned char*)malloc((size_t)E);
+    if (!z || !p || !taken) {
+        free(z); free(p); free(taken);
+        return -1;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        /* scores */
+        for (int64_t e = 0; e < E; ++e) {
+            float b = (bias && g_mutation != MUT_TOPK_NO_BIAS) ? bias[e] : 0.0f;
+            z[e] = logits[t * E + e] + b;      /* one fp32 addition */
+        }
+        /* softmax */
+        double zmax = z[0];
+        for (int64_t e = 1; e < E; ++e)
+            if (z[e] > zmax) zmax = z[e];
+        double denom = 0.0;
+        for (int64_t e = 0; e < E; ++e) {
+            p[e] = exp((double)z[e] - zmax);
+            denom += p[e];
+        }
+        for (int64_t e = 0; e < E; ++e) p[e] /= denom;
+        /* top-k */
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || z[e] > z[best] ||
+                    (g_mutation == MUT_TOPK_TIE_HIGH && z[e] == z[best]))
+                    best = e;
+            }
+            taken[best] = 1;
+            ids[t * k + j] = (int32_t)best;
+        }
+        /* renormalisation over the chosen k */
+        double sel = 0.0;
+        for (int j = 0; j < k; ++j) sel += p[ids[t * k + j]];
+        for (int j = 0; j < k; ++j) {
+            double w = g_mutation == MUT_TOPK_NO_RENORM ? p[ids[t * k + j]] : p[ids[t * k + j]] / sel;
+            weights[t * k + j] = (float)w;
+        }
+    }
+    free(z); free(p); free(taken);
     return 0;
 }
 

@@ -321,10 +321,53 @@ def pin_split_routing_weight(oracle):
         assert np.array_equal(_bf16_to_f64(_run(oracle, c3)), 0.5 * _bf16_to_f64(one))
 
 
+def pin_router(oracle):
+    """Router: ids are numpy's stable argsort of the fp32 scores (ties to the
+    lower index); weights match scipy's softmax renormalised over the chosen
+    experts; closed forms (k = 1 gives weight 1, all-equal scores give 1/k in
+    index order, two scores ln 3 apart give 3/4 and 1/4, k = E is the full
+    softmax); a constant shift changes nothing; a bias of -1e4 removes an
+    expert."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(21)
+    for T, E, k, with_bias in ((5, 8, 2, False), (7, 64, 8, True), (3, 256, 8, True), (2, 5, 5, False)):
+        lg = rng.standard_normal((T, E), dtype=np.float32)
+        bias = (-1.1 * np.log(np.arange(1, E + 1))).astype(np.float32) if with_bias else None
+        ids, w = oracle.route_topk(lg, k, bias)
+        z = lg + (bias if with_bias else np.float32(0))
+        assert z.dtype == np.float32
+        assert np.array_equal(ids, np.argsort(-z, axis=1, kind="stable")[:, :k])
+        p = softmax(z.astype(np.float64), axis=1)
+        sel = np.take_along_axis(p, ids.astype(np.int64), axis=1)
+        ref = (sel / sel.sum(axis=1, keepdims=True)).astype(np.float32)
+        assert np.max(np.abs(w.astype(np.float64) - ref) / ref) <= 2 * 2.0 ** -24, (T, E, k)
+        assert np.all(np.abs(w.sum(axis=1) - 1.0) <= k * 2.0 ** -24)
+        if k == E:
+            assert np.allclose(w, softmax(z.astype(np.float64), axis=1)[np.arange(T)[:, None], ids], rtol=3e-7)
+        # an exact constant shift (scores are multiples of 2^-10 below 16)
+        q = np.round(lg * 1024) / 1024
+        a = oracle.route_topk(q.astype(np.float32), k, bias)
+        b = oracle.route_topk((q + 3.0).astype(np.float32), k, bias)
+        assert np.array_equal(a[0], b[0])
+        assert np.max(np.abs(a[1].astype(np.float64) - b[1])) <= 2.0 ** -23
+    ids, w = oracle.route_topk(np.zeros((2, 6), np.float32), 3)
+    assert ids.tolist() == [[0, 1, 2], [0, 1, 2]] and np.all(w == np.float32(1 / 3))
+    ids, w = oracle.route_topk(np.array([[0.5, -2.0, 0.7, 0.1]], np.float32), 1)
+    assert ids.tolist() == [[2]] and w[0, 0] == 1.0
+    lg = np.array([[-3.0, 1.0, 1.0 - math.log(3.0), -5.0]], np.float32)
+    ids, w = oracle.route_topk(lg, 2)
+    assert ids.tolist() == [[1, 2]]
+    assert abs(float(w[0, 0]) - 0.75) <= 2e-7 and abs(float(w[0, 1]) - 0.25) <= 2e-7
+    bias = np.zeros(6, np.float32)
+    bias[[0, 1, 2]] = -1e4
+    ids, _ = oracle.route_topk(np.zeros((1, 6), np.float32), 3, bias)
+    assert ids.tolist() == [[3, 4, 5]]
+
+
 PINS = [pin_fp16_decode, pin_bf16_rounding, pin_hand_words, pin_pack_roundtrip, pin_dequant,
         pin_route, pin_zero_codes, pin_brute_force, pin_dense_mlp, pin_clamp_closed_form,
         pin_scale_doubling, pin_relabel_and_token_permutation, pin_split_routing_weight, pin_fp32_mode,
-        pin_given_h]
+        pin_given_h, pin_router]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
