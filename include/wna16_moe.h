@@ -119,6 +119,24 @@ WNA16_API int wna16_moe_forward(const void* x, const int32_t* topk_ids, const fl
  * WNA16_ERR_CUDA. */
 WNA16_API int wna16_moe_read_status(const void* workspace, int* device_status, void* stream);
 
+/* Router: the step that produces topk_ids / topk_weights from router logits
+ * (the workloads' "top-k softmax routing from N(0,1) logits", renormalised,
+ * with the expert-popularity skew entering as a logit bias).  Per token t:
+ *   z_e  = logits[t][e] + bias[e]                (one fp32 addition; bias may be NULL)
+ *   ids  = the topk experts of largest z, descending; equal z -> lower index
+ *          (the order of softmax(z), since exp is increasing)
+ *   w_j  = softmax(z) renormalised over the chosen experts
+ *        = exp(z_j - z_max) / sum_i exp(z_i - z_max)       (fp32, i in choice order)
+ *   logits        fp32 device [T, E], finite
+ *   bias          fp32 device [E] or NULL
+ *   topk_ids      int32 device [T, topk] (written)
+ *   topk_weights  fp32 device [T, topk] (written)
+ * 1 <= topk <= min(E, 32); E <= 1024.  Asynchronous on `stream`; returns
+ * WNA16_OK, WNA16_ERR_INVALID_ARG, WNA16_ERR_UNSUPPORTED or WNA16_ERR_CUDA
+ * (nothing launched on a non-zero return other than WNA16_ERR_CUDA). */
+WNA16_API int wna16_moe_route_topk(const float* logits, const float* bias, int64_t T, int64_t E, int topk,
+                                   int32_t* topk_ids, float* topk_weights, void* stream);
+
 /* Message for the last host-side error on the calling thread ("" if none). */
 WNA16_API const char* wna16_moe_last_error(void);
 

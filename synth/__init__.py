@@ -103,11 +103,21 @@ def to_bf16_bits(a: np.ndarray) -> np.ndarray:
     return t.view(torch.int16).numpy().view(np.uint16)
 
 
-def make_routing(w: Workload, seed: int = 0):
+def make_logits(w: Workload, seed: int = 0):
+    """Router logits fp32 [T, E] ~ N(0, 1) and the popularity bias fp32 [E]
+    (-s*ln(e+1) for a Zipf(s) workload, else None)."""
     rng = _streams(seed)[0]
     logits = rng.standard_normal((w.T, w.E), dtype=np.float32)
+    bias = None
     if w.zipf_s:
-        logits = logits + (-w.zipf_s * np.log(np.arange(1, w.E + 1, dtype=np.float64))).astype(np.float32)
+        bias = (-w.zipf_s * np.log(np.arange(1, w.E + 1, dtype=np.float64))).astype(np.float32)
+    return logits, bias
+
+
+def make_routing(w: Workload, seed: int = 0):
+    logits, bias = make_logits(w, seed)
+    if bias is not None:
+        logits = logits + bias
     return route_topk(logits, w.topk)
 
 

@@ -19,7 +19,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = binding.exported_names_in_header()
-    assert len(names) == 14, names
+    assert len(names) == 15, names
     for n in names:
         assert hasattr(lib, n), n
 

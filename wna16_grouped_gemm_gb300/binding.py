@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH):
     lib.wna16_moe_profile.argtypes = [I]
     lib.wna16_moe_profile_read.restype = I
     lib.wna16_moe_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), I]
+    lib.wna16_moe_route_topk.restype = I
+    lib.wna16_moe_route_topk.argtypes = [P, P, I64, I64, I, P, P, P]
     lib.wna16_moe_combine.restype = I
     lib.wna16_moe_combine.argtypes = [P, P, I64, I64, I, I64, I64, I, P, P, SZ, P]
     _lib = lib
@@ -194,6 +196,25 @@ def forward_noalloc(x, topk_ids, topk_weights, w13_packed, w13_scales, w2_packed
         _ptr(w2_scales), T, K, N, E, topk, group_size, group_size_w2, bits, float(swiglu_limit), _ptr(out),
         _stream(stream)))
     return out
+
+
+def route_topk(logits, topk: int, bias=None, ids=None, weights=None, stream=None):
+    """Router: (topk_ids int32 [T, topk], topk_weights fp32 [T, topk]) from
+    fp32 logits [T, E] (+ bias [E]): softmax, top-k (ties to the lower
+    index), renormalised."""
+    _need(logits, torch.float32, "logits", 2)
+    T, E = logits.shape
+    if bias is not None:
+        _need(bias, torch.float32, "bias", 1)
+    if ids is None:
+        ids = torch.empty(T, topk, dtype=torch.int32, device=logits.device)
+    if weights is None:
+        weights = torch.empty(T, topk, dtype=torch.float32, device=logits.device)
+    _need(ids, torch.int32, "ids", 2)
+    _need(weights, torch.float32, "weights", 2)
+    _check(load_library().wna16_moe_route_topk(_ptr(logits), _ptr(bias), T, E, topk, _ptr(ids), _ptr(weights),
+                                               _stream(stream)))
+    return ids, weights
 
 
 STAGES = ("route", "gather", "w13", "w2", "combine")

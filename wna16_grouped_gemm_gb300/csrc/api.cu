@@ -536,6 +536,27 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     return WNA16_OK;
 }
 
+int wna16_moe_route_topk(const float* logits, const float* bias, int64_t T, int64_t E, int topk, int32_t* topk_ids,
+                         float* topk_weights, void* stream) {
+    g_err[0] = 0;
+    if (T < 0 || E <= 0) return fail(WNA16_ERR_INVALID_ARG, "T=%lld must be >= 0 and E=%lld > 0", (long long)T,
+                                     (long long)E);
+    if (E > 1024) return fail(WNA16_ERR_UNSUPPORTED, "E=%lld: at most 1024 experts", (long long)E);
+    if (topk < 1 || topk > E || topk > 32)
+        return fail(WNA16_ERR_INVALID_ARG, "topk=%d must be in [1, min(E, 32)]", topk);
+    if (T * E >= (int64_t(1) << 40) || T >= (int64_t(1) << 31))
+        return fail(WNA16_ERR_UNSUPPORTED, "T=%lld too large", (long long)T);
+    if (T == 0) return WNA16_OK;
+    if (int rc = check_ptr(logits, 4, "logits")) return rc;
+    if (bias)
+        if (int rc = check_ptr(bias, 4, "bias")) return rc;
+    if (int rc = check_ptr(topk_ids, 4, "topk_ids")) return rc;
+    if (int rc = check_ptr(topk_weights, 4, "topk_weights")) return rc;
+    cudaError_t e = launch_route_topk(logits, bias, static_cast<int>(T), static_cast<int>(E), topk, topk_ids,
+                                      topk_weights, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "router kernel launch");
+}
+
 int wna16_moe_launches_last_forward(void) { return g_launches; }
 
 int wna16_moe_profile(int slots) {

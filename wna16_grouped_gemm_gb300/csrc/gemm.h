@@ -65,6 +65,10 @@ cudaError_t ensure_dynamic_smem(const void* fn, int bytes);
 // Routing / gather / combine / pack kernels (kernels.cu).
 cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
                          int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream);
+// Router: ids/weights [T, k] from fp32 logits [T, E] (+ bias [E] or null);
+// 1 <= k <= min(E, 32), E <= 1024.
+cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
+                              float* weights, cudaStream_t stream);
 // With csum (2-bit interleaved order only, group 128): also the offset-code
 // corrections of the gathered rows, csum[g * R + i] = sum over group g of w(k) x.
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,

@@ -146,6 +146,69 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
 }
 
+// Router: one warp per token.  Lane l holds the scores z = logit + bias of
+// experts l, l + 32, ... (PL per lane).  k rounds of a warp-wide argmax (the
+// larger score wins, equal scores go to the lower expert index) pick the
+// experts in descending order; the weights are the softmax renormalised over
+// the chosen k, exp(z_j - z_max) / sum_i exp(z_i - z_max), which equals the
+// full softmax divided by its sum over the chosen experts.  Lane j keeps the
+// j-th choice; the sum runs in choice order.
+template <int PL>
+__global__ void __launch_bounds__(256)
+    route_topk_kernel(const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+                      int32_t* __restrict__ ids, float* __restrict__ weights) {
+    pdl_wait();
+    pdl_trigger();
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;   // whole warps leave together
+    const float* row = logits + static_cast<int64_t>(t) * E;
+    float z[PL];
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+        const int e = i * 32 + lane;
+        z[i] = e < E ? __fadd_rn(__ldg(row + e), bias ? __ldg(bias + e) : 0.0f) : 0.0f;
+    }
+    uint32_t taken = 0;
+    float my_z = 0.0f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = 0.0f;
+        int bi = -1;
+#pragma unroll
+        for (int i = 0; i < PL; ++i) {
+            const int e = i * 32 + lane;
+            if (e < E && !((taken >> i) & 1u) && (bi < 0 || z[i] > bv)) {
+                bv = z[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (oi >= 0 && (bi < 0 || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        // k <= E, so a candidate always exists; the owner marks it taken
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+            my_z = bv;
+            my_id = bi;
+        }
+    }
+    const float zmax = __shfl_sync(0xffffffffu, my_z, 0);
+    const float ex = lane < k ? expf(my_z - zmax) : 0.0f;
+    float sum = 0.0f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xffffffffu, ex, j);
+    if (lane < k) {
+        ids[static_cast<int64_t>(t) * k + lane] = my_id;
+        weights[static_cast<int64_t>(t) * k + lane] = ex / sum;
+    }
+}
+
 // 16 BF16 (elements 0..15 of a block, as two 8-element vectors) -> the
 // interleaved order (0, 8, 1, 9, ..., 7, 15), and back.
 __device__ __forceinline__ void interleave_block(const uint4& lo, const uint4& hi, uint4& a, uint4& b) {
@@ -439,6 +502,22 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, 
     route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, nt, counts, offsets, perm, inv, tiles, n_tiles,
                                                     status);
     return cudaGetLastError();
+}
+
+cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
+                              float* weights, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    const dim3 grid((T + 7) / 8), block(256);
+    const int pl = (E + 31) / 32;
+    if (pl <= 1) return launch_pdl(route_topk_kernel<1>, grid, block, 0, stream, logits, bias, T, E, k, ids, weights);
+    if (pl <= 2) return launch_pdl(route_topk_kernel<2>, grid, block, 0, stream, logits, bias, T, E, k, ids, weights);
+    if (pl <= 4) return launch_pdl(route_topk_kernel<4>, grid, block, 0, stream, logits, bias, T, E, k, ids, weights);
+    if (pl <= 8) return launch_pdl(route_topk_kernel<8>, grid, block, 0, stream, logits, bias, T, E, k, ids, weights);
+    if (pl <= 16)
+        return launch_pdl(route_topk_kernel<16>, grid, block, 0, stream, logits, bias, T, E, k, ids, weights);
+    if (pl <= 32)
+        return launch_pdl(route_topk_kernel<32>, grid, block, 0, stream, logits, bias, T, E, k, ids, weights);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
