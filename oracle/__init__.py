@@ -78,6 +78,10 @@ def _load():
     lib.oracle_forward.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I, I64, I64, I,
                                    ctypes.c_float, I, P, I64, P, P, P, P]
     lib.oracle_forward.restype = I
+    lib.oracle_combine_partial.argtypes = [P, P, P, I64, I64, I, I64, I64, P]
+    lib.oracle_combine_partial.restype = I
+    lib.oracle_sum_partials.argtypes = [P, I, I64, P]
+    lib.oracle_sum_partials.restype = I
     lib.oracle_route_topk.argtypes = [P, P, I64, I64, I, P, P]
     lib.oracle_route_topk.restype = I
     lib.oracle_num_threads.argtypes = []
@@ -223,3 +227,32 @@ def route_topk(logits: np.ndarray, k: int, bias: np.ndarray | None = None):
     if _load().oracle_route_topk(_ptr(lg), _ptr(b), T, E, k, _ptr(ids), _ptr(w)) != 0:
         raise OracleError("route_topk: k must be in [1, E]")
     return ids, w
+
+
+def combine_partial(ids: np.ndarray, weights: np.ndarray, y_bf16: np.ndarray, expert_range) -> np.ndarray:
+    """Expert-parallel partial output of one rank: fp32 [n, K] = sum over the
+    slots routed to experts in [begin, end) of w * y (fp64, rounded once to
+    fp32), slots in order.  y is the BF16 bits of the down projection per
+    slot t*topk + j ([n*topk, K], e.g. forward(..., return_intermediates=True))."""
+    ids = _c(ids, np.int32)
+    wts = _c(weights, np.float32)
+    y = _c(y_bf16, np.uint16)
+    n, topk = ids.shape
+    K = y.shape[1]
+    if y.shape[0] != n * topk:
+        raise OracleError("y must be [n*topk, K]")
+    out = np.empty((n, K), np.float32)
+    b, e = expert_range
+    if _load().oracle_combine_partial(_ptr(ids), _ptr(wts), _ptr(y), n, K, topk, int(b), int(e), _ptr(out)) != 0:
+        raise OracleError("combine_partial: bad arguments")
+    return out
+
+
+def sum_partials(partials) -> np.ndarray:
+    """bf16 bits of the fp32 sum of the ranks' partial outputs, ranks added in order."""
+    p = _c(np.stack(partials), np.float32)
+    P = p.shape[0]
+    out = np.empty(p.shape[1:], np.uint16)
+    if _load().oracle_sum_partials(_ptr(p), P, int(np.prod(p.shape[1:])), _ptr(out)) != 0:
+        raise OracleError("sum_partials: bad arguments")
+    return out

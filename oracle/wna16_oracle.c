@@ -453,6 +453,56 @@ int oracle_forward(const uint16_t* x, const int32_t* ids, const float* wts,
 }
 
 /* ------------------------------------------------------------------ */
+/* Expert-parallel profile: partial outputs per expert range, summed in   */
+/* rank order.                                                           */
+/* ------------------------------------------------------------------ */
+
+/*
+ * When the experts are split across ranks (each rank holds the experts
+ * [e_begin, e_end) and runs the path on them alone), rank r's combine covers
+ * only the slots routed to its experts and is kept in fp32 for the reduction
+ * across ranks:
+ *
+ *   partial_r[t][m] = fp32( sum_{j ascending, e_begin <= ids[t][j] < e_end} w[t][j] * y[t*topk+j][m] )
+ *   out[t][m]       = bf16( (((partial_0 + partial_1) + partial_2) + ...) )   each + in fp32
+ *
+ * y is the BF16 down-projection output of step 6 (computed per slot, here
+ * given as BF16 bits [n*topk, K]); the partial sum is fp64, rounded once to
+ * fp32.  This changes one rounding point of the single-device combine (the
+ * fp32 partials before the final BF16 rounding), so it is its own profile.
+ * ids/wts [n, topk]; partial fp32 [n, K].
+ */
+int oracle_combine_partial(const int32_t* ids, const float* wts, const uint16_t* y, int64_t n, int64_t K,
+                           int topk, int64_t e_begin, int64_t e_end, float* partial)
+{
+    if (n < 0 || K <= 0 || topk <= 0 || e_begin > e_end) return -1;
+    for (int64_t t = 0; t < n; ++t)
+        for (int64_t m = 0; m < K; ++m) {
+            double acc = 0.0;
+            for (int j = 0; j < topk; ++j) {
+                int32_t e = ids[t * topk + j];
+                if (e < e_begin || e >= e_end) continue;
+                acc += (double)wts[t * topk + j] * oracle_bf16_to_double(y[(t * topk + j) * K + m]);
+            }
+            partial[t * K + m] = (float)acc;
+        }
+    return 0;
+}
+
+/* out = bf16( partial_0 + partial_1 + ... ) with the ranks added in order in
+ * fp32; partials fp32 [P][count]. */
+int oracle_sum_partials(const float* partials, int P, int64_t count, uint16_t* out)
+{
+    if (P <= 0 || count < 0) return -1;
+    for (int64_t q = 0; q < count; ++q) {
+        float s = partials[q];
+        for (int r = 1; r < P; ++r) s = s + partials[(int64_t)r * count + q];
+        out[q] = oracle_bf16_rne((double)s);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* Router: softmax over the experts, top-k, renormalisation.             */
 /* ------------------------------------------------------------------ */
 
