@@ -113,6 +113,31 @@ WNA16_API int wna16_moe_forward(const void* x, const int32_t* topk_ids, const fl
                       int group_size, int group_size_w2, int bits, float swiglu_limit,
                       void* out, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Expert-parallel partial forward: the experts are split across devices and
+ * this call runs the path for the local ones, [expert_begin, expert_begin +
+ * E_local) of E_total, only (the expert-parallel deployment of the page
+ * "Incubate DeepSeek V4 WNA16 runtime on SM86", section "Measured server60
+ * result", shards the same layer across four GPUs; here the experts, not the
+ * intermediate dimension, are split).  The weight pointers hold the local
+ * experts only ([E_local, ...], local expert i = global expert
+ * expert_begin + i); topk_ids hold global ids in [0, E_total).  A slot whose
+ * expert is not local contributes nothing.  Output:
+ *   out_partial fp32 device [T, K] = sum over the slots t*topk + j with a
+ *                local expert (j ascending, fp32) of topk_weights[t][j] * y
+ *                where y = bf16(W2 h) as in wna16_moe_forward; not rounded to
+ *                BF16, so that the ranks' partials can be summed (in rank
+ *                order, fp32) before the final BF16 rounding.
+ * Workspace: wna16_moe_workspace_size(T, K, N, E_local, topk, bits).  Other
+ * arguments, limits and errors as for wna16_moe_forward (topk <= E_total;
+ * E_local <= 1024). */
+WNA16_API int wna16_moe_forward_partial(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                                        const int32_t* w13_packed, const uint16_t* w13_scales,
+                                        const int32_t* w2_packed, const uint16_t* w2_scales,
+                                        int64_t T, int64_t K, int64_t N, int64_t E_total, int64_t expert_begin,
+                                        int64_t E_local, int topk, int group_size, int group_size_w2, int bits,
+                                        float swiglu_limit, float* out_partial, void* workspace,
+                                        size_t workspace_bytes, void* stream);
+
 /* Synchronise `stream` and read the device status word of the last call that
  * used `workspace` (WNA16_OK, WNA16_ERR_BAD_ROUTING or
  * WNA16_ERR_DEVICE_TIMEOUT) into *device_status.  Returns WNA16_OK or

@@ -70,6 +70,10 @@ WORKLOADS = {
     "prefill_w4_g64": Workload("prefill_w4_g64", T=8192, K=4096, N=2048, E=256, topk=8, bits=4,
                                g13=128, g2=64, scale_lo=0.001, scale_hi=0.005),
 }
+# one GPU's share of the tensor-parallel deployment the pages measure (TP 4
+# over the intermediate dimension: w13 rows and w2 columns split four ways)
+WORKLOADS["decode_w2_tp4"] = dataclasses.replace(WORKLOADS["decode_w2"], name="decode_w2_tp4", N=512)
+WORKLOADS["prefill_w2_zipf_tp4"] = dataclasses.replace(WORKLOADS["prefill_w2_zipf"], name="prefill_w2_zipf_tp4", N=512)
 
 
 def get(name: str) -> Workload:

@@ -19,7 +19,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = binding.exported_names_in_header()
-    assert len(names) == 15, names
+    assert len(names) == 16, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -134,3 +134,29 @@ def test_missing_library_fails_loudly(tmp_path):
             binding.load_library(str(tmp_path / "nope.so"))
     finally:
         binding._lib = saved
+
+
+def test_partial_forward_rejects_on_host(lib):
+    P = ctypes.c_void_p
+    f = lib.wna16_moe_forward_partial
+
+    def call(E_total=256, begin=0, E_local=128, topk=8, out=P(0x90000)):
+        return f(A16, A16, A16, A16, A16, A16, A16, 4, 4096, 2048, E_total, begin, E_local, topk, 128, 0, 2,
+                 ctypes.c_float(7.0), out, P(0x100000), 1 << 40, None)
+    assert call(begin=200) == binding.ERR_INVALID_ARG          # range past E_total
+    assert call(begin=-1) == binding.ERR_INVALID_ARG
+    assert call(E_local=300) == binding.ERR_INVALID_ARG         # more local experts than exist
+    assert call(topk=300) == binding.ERR_INVALID_ARG            # topk > E_total
+    assert call(out=None) == binding.ERR_INVALID_ARG
+    assert call(out=P(0x10000 + 4096)) == binding.ERR_INVALID_ARG   # fp32 out overlaps x
+
+
+def test_router_rejects_on_host(lib):
+    P = ctypes.c_void_p
+    f = lib.wna16_moe_route_topk
+    assert f(A16, None, 4, 256, 33, A16, A16, None) == binding.ERR_INVALID_ARG     # topk > 32
+    assert f(A16, None, 4, 8, 9, A16, A16, None) == binding.ERR_INVALID_ARG       # topk > E
+    assert f(A16, None, 4, 2048, 8, A16, A16, None) == binding.ERR_UNSUPPORTED    # E > 1024
+    assert f(None, None, 4, 256, 8, A16, A16, None) == binding.ERR_INVALID_ARG
+    assert f(A16, P(0x10002), 4, 256, 8, A16, A16, None) == binding.ERR_INVALID_ARG  # misaligned bias
+    assert f(None, None, 0, 256, 8, None, None, None) == binding.OK

@@ -58,3 +58,57 @@ def test_torchrun_two_ranks_one_json_line():
     rec = json.loads(lines[0])
     assert rec["impl"] == "reference" and rec["n_gpus"] == 2 and rec["value"] > 0
     assert rec["cpu_baseline"]["kind"] == "oracle"
+
+
+def _ep_worker(rank, world, port, q):
+    """Rank `rank` holds experts [rank*E/2, (rank+1)*E/2): the oracle's partial
+    for them, summed across the two ranks with gloo and rounded to BF16."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    sys.path.insert(0, ROOT)
+    import numpy as np
+    import torch
+    import oracle
+    import synth
+    w = synth.get("tiny_w2")
+    inp = synth.make_all(w, 0)
+    _, _, y = oracle.forward(inp["x"], inp["ids"], inp["weights"], inp["w13_packed"], inp["w13_scales"],
+                             inp["w2_packed"], inp["w2_scales"], bits=w.bits, group_size=w.g13,
+                             group_size_w2=w.g2, swiglu_limit=w.swiglu_limit, return_intermediates=True)
+    half = w.E // world
+    part = torch.from_numpy(oracle.combine_partial(inp["ids"], inp["weights"], y, (rank * half, (rank + 1) * half)))
+    dist.all_reduce(part, op=dist.ReduceOp.SUM)
+    out = part.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    q.put((rank, out.tobytes()))
+    dist.destroy_process_group()
+
+
+def test_expert_parallel_sum_gloo():
+    """Two gloo ranks each run the oracle's expert-parallel partial for half the
+    experts; the all-reduced sum, rounded to BF16, is the oracle's
+    expert-parallel profile (partials summed in rank order) bit for bit -- with
+    two ranks the fp32 sum has one addition, so its order cannot differ."""
+    import numpy as np
+    import oracle
+    import synth
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ep_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    w = synth.get("tiny_w2")
+    inp = synth.make_all(w, 0)
+    _, _, y = oracle.forward(inp["x"], inp["ids"], inp["weights"], inp["w13_packed"], inp["w13_scales"],
+                             inp["w2_packed"], inp["w2_scales"], bits=w.bits, group_size=w.g13,
+                             group_size_w2=w.g2, swiglu_limit=w.swiglu_limit, return_intermediates=True)
+    parts = [oracle.combine_partial(inp["ids"], inp["weights"], y, (0, w.E // 2)),
+             oracle.combine_partial(inp["ids"], inp["weights"], y, (w.E // 2, w.E))]
+    profile = oracle.sum_partials(parts)
+    for r in (0, 1):
+        got = np.frombuffer(res[r], np.uint16).reshape(profile.shape)
+        assert np.array_equal(got, profile)

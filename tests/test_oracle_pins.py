@@ -364,10 +364,44 @@ def pin_router(oracle):
     assert ids.tolist() == [[3, 4, 5]]
 
 
+def pin_ep_profile(oracle):
+    """Expert-parallel profile: an expert range with no routed slot gives +0;
+    a top-1 slot of weight 1 gives its y exactly; partials over disjoint
+    ranges that cover all experts add up (fp32) to the partial over all of
+    them; BF16 of the all-expert partial equals the single-device output but
+    for rare double-rounding cases; the rank sum adds in rank order in fp32
+    (numpy float32 arithmetic) and rounds like torch's fp32 -> bf16."""
+    for bits in (2, 4):
+        c = _tiny_case(bits, T=5, K=64, N=32, E=4, topk=2)
+        out, _, y = _run(oracle, c, return_intermediates=True)
+        E = c["E"]
+        assert np.all(oracle.combine_partial(c["ids"], c["weights"], y, (E, E)) == 0.0)
+        unused = [e for e in range(E) if e not in set(c["ids"].ravel().tolist())]
+        for e in unused:
+            assert np.all(oracle.combine_partial(c["ids"], c["weights"], y, (e, e + 1)) == 0.0)
+        full = oracle.combine_partial(c["ids"], c["weights"], y, (0, E))
+        parts = [oracle.combine_partial(c["ids"], c["weights"], y, r) for r in ((0, 1), (1, 3), (3, E))]
+        s = (parts[0] + parts[1]) + parts[2]
+        mag = np.abs(parts[0]).astype(np.float64) + np.abs(parts[1]) + np.abs(parts[2])
+        assert np.all(np.abs(s.astype(np.float64) - full) <= 4 * 2.0 ** -24 * mag)
+        fb = torch.from_numpy(full).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        diff = np.abs(fb.astype(np.int32) - out.astype(np.int32))
+        assert diff.max() <= 1 and (diff == 0).mean() >= 0.99
+        got = oracle.sum_partials(parts)
+        ref32 = (parts[0].astype(np.float32) + parts[1].astype(np.float32)) + parts[2].astype(np.float32)
+        assert np.array_equal(got, torch.from_numpy(ref32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    c = _tiny_case(2, T=3, K=64, N=32, E=3, topk=1)
+    c["weights"] = np.ones((3, 1), np.float32)
+    _, _, y = _run(oracle, c, return_intermediates=True)
+    p = oracle.combine_partial(c["ids"], c["weights"], y, (0, 3))
+    assert np.array_equal(p, _bf16_to_f64(y).astype(np.float32))
+    assert np.all(oracle.sum_partials([p, -p]) == 0)
+
+
 PINS = [pin_fp16_decode, pin_bf16_rounding, pin_hand_words, pin_pack_roundtrip, pin_dequant,
         pin_route, pin_zero_codes, pin_brute_force, pin_dense_mlp, pin_clamp_closed_form,
         pin_scale_doubling, pin_relabel_and_token_permutation, pin_split_routing_weight, pin_fp32_mode,
-        pin_given_h, pin_router]
+        pin_given_h, pin_router, pin_ep_profile]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])

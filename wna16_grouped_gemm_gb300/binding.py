@@ -78,6 +78,9 @@ def load_library(path: str = LIB_PATH):
     lib.wna16_moe_profile.argtypes = [I]
     lib.wna16_moe_profile_read.restype = I
     lib.wna16_moe_profile_read.argtypes = [ctypes.POINTER(ctypes.c_float), I]
+    lib.wna16_moe_forward_partial.restype = I
+    lib.wna16_moe_forward_partial.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, I, I, F, P,
+                                              P, SZ, P]
     lib.wna16_moe_route_topk.restype = I
     lib.wna16_moe_route_topk.argtypes = [P, P, I64, I64, I, P, P, P]
     lib.wna16_moe_combine.restype = I
@@ -171,6 +174,39 @@ def forward(x, topk_ids, topk_weights, w13_packed, w13_scales, w2_packed, w2_sca
         _ptr(w2_scales), T, K, N, E, topk, group_size, group_size_w2, bits, float(swiglu_limit), _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream))
     _check(rc)
+    return out
+
+
+def forward_partial(x, topk_ids, topk_weights, w13_local, w13_scales_local, w2_local, w2_scales_local, *,
+                    expert_begin: int, E_total: int, bits: int, group_size: int, group_size_w2: int = 0,
+                    swiglu_limit: float = 7.0, out=None, workspace=None, stream=None) -> torch.Tensor:
+    """Expert-parallel partial forward over the local experts [expert_begin,
+    expert_begin + E_local) (the weight tensors hold those experts only);
+    returns the fp32 partial output [T, K] (unrounded, to be summed across
+    ranks in rank order and then rounded to BF16)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(topk_ids, torch.int32, "topk_ids", 2)
+    _need(topk_weights, torch.float32, "topk_weights", 2)
+    _need(w13_local, torch.int32, "w13_local", 3)
+    _need(w2_local, torch.int32, "w2_local", 3)
+    _need(w13_scales_local, torch.float16, "w13_scales_local", 3)
+    _need(w2_scales_local, torch.float16, "w2_scales_local", 3)
+    T, K = x.shape
+    topk = topk_ids.shape[1]
+    E_local = w13_local.shape[0]
+    N = w13_local.shape[1] // 2
+    p = 32 // bits
+    if tuple(w13_local.shape) != (E_local, 2 * N, K // p) or tuple(w2_local.shape) != (E_local, K, N // p):
+        raise ValueError("local weight shapes must be [E_local, 2N, K/p] and [E_local, K, N/p]")
+    if out is None:
+        out = torch.empty(T, K, dtype=torch.float32, device=x.device)
+    _need(out, torch.float32, "out", 2)
+    if workspace is None:
+        workspace = alloc_workspace(T, K, N, E_local, topk, bits, x.device)
+    _check(load_library().wna16_moe_forward_partial(
+        _ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(w13_local), _ptr(w13_scales_local), _ptr(w2_local),
+        _ptr(w2_scales_local), T, K, N, E_total, expert_begin, E_local, topk, group_size, group_size_w2, bits,
+        float(swiglu_limit), _ptr(out), _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

@@ -278,8 +278,11 @@ int check_workspace(const void* ws, size_t bytes, const Layout& L) {
 
 // ---------------------------------------------------------------- launch helpers
 
-int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStream_t s) {
-    cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), L.nt, at<int>(ws, L.counts),
+// Routing lists of the local experts [e_begin, e_begin + E) among E_total.
+int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStream_t s, int64_t e_begin = 0,
+              int64_t E_total = -1) {
+    cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), static_cast<int>(e_begin),
+                                 static_cast<int>(E_total < 0 ? E : E_total), L.nt, at<int>(ws, L.counts),
                                  at<int>(ws, L.offsets), at<int>(ws, L.perm), at<int>(ws, L.inv),
                                  at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status), s);
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "route kernel launch");
@@ -459,12 +462,25 @@ int wna16_moe_check_wait_timeout(void* workspace, size_t workspace_bytes, int64_
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "wait check kernel launch");
 }
 
-int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_weights, const int32_t* w13_packed,
-                      const uint16_t* w13_scales, const int32_t* w2_packed, const uint16_t* w2_scales, int64_t T,
-                      int64_t K, int64_t N, int64_t E, int topk, int group_size, int group_size_w2, int bits,
-                      float swiglu_limit, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The forward over the local experts [e_begin, e_begin + E) of E_total (all
+// of them on a single device): bf16 out, or with f32_out the fp32 partial
+// output of that expert range.
+int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weights, const int32_t* w13_packed,
+                 const uint16_t* w13_scales, const int32_t* w2_packed, const uint16_t* w2_scales, int64_t T, int64_t K,
+                 int64_t N, int64_t E, int64_t e_begin, int64_t E_total, int topk, int group_size, int group_size_w2,
+                 int bits, float swiglu_limit, void* out, bool f32_out, void* workspace, size_t workspace_bytes,
+                 void* stream) {
     g_err[0] = 0;
-    if (int rc = check_dims(T, K, N, E, topk, bits)) return rc;
+    if (int rc = check_dims(T, K, N, E, f32_out ? 1 : topk, bits)) return rc;
+    if (topk <= 0) return fail(WNA16_ERR_INVALID_ARG, "topk=%d must be positive", topk);
+    if (e_begin < 0 || E_total < E || e_begin > E_total - E || E_total >= (int64_t(1) << 31))
+        return fail(WNA16_ERR_INVALID_ARG, "expert range [%lld, %lld) is not inside [0, %lld)", (long long)e_begin,
+                    (long long)(e_begin + E), (long long)E_total);
+    if (topk > E_total) return fail(WNA16_ERR_INVALID_ARG, "topk=%d exceeds E=%lld", topk, (long long)E_total);
     const int g2 = group_size_w2 ? group_size_w2 : group_size;
     if (int rc = check_group(group_size, K, "group_size")) return rc;
     if (int rc = check_group(g2, N, "group_size_w2")) return rc;
@@ -472,6 +488,7 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     if (T == 0) return WNA16_OK;
     if (int rc = check_ptr(x, 16, "x")) return rc;
     if (int rc = check_ptr(out, 16, "out")) return rc;
+    if (T * topk >= (int64_t(1) << 31)) return fail(WNA16_ERR_UNSUPPORTED, "T*topk must be < 2^31");
     if (int rc = check_ptr(topk_ids, 4, "topk_ids")) return rc;
     if (int rc = check_ptr(topk_weights, 4, "topk_weights")) return rc;
     if (int rc = check_ptr(w13_packed, 16, "w13_packed")) return rc;
@@ -480,8 +497,9 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     if (int rc = check_ptr(w2_scales, 2, "w2_scales")) return rc;
     {
         const uintptr_t xb = reinterpret_cast<uintptr_t>(x), ob = reinterpret_cast<uintptr_t>(out);
-        const uintptr_t bytes = static_cast<uintptr_t>(T * K * 2);
-        if (xb < ob + bytes && ob < xb + bytes) return fail(WNA16_ERR_INVALID_ARG, "out overlaps x");
+        const uintptr_t xbytes = static_cast<uintptr_t>(T * K * 2);
+        const uintptr_t obytes = static_cast<uintptr_t>(T * K * (f32_out ? 4 : 2));
+        if (xb < ob + obytes && ob < xb + xbytes) return fail(WNA16_ERR_INVALID_ARG, "out overlaps x");
     }
     const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
@@ -503,7 +521,7 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
         return rc;
 
     mark(0, s);
-    if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
+    if (int rc = run_route(topk_ids, E, L, workspace, s, e_begin, E_total)) return rc;
     mark(1, s);
     cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
@@ -524,16 +542,44 @@ int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_
     mark(4, s);
     if (p2.gp.ksplit > 1)      // split K: the combine adds the splits itself
         e = launch_combine_partials(at<float>(workspace, L.partial), p2.gp.ksplit, static_cast<int>(L.R), topk_weights,
-                                    at<int>(workspace, L.inv), static_cast<int>(T), topk, static_cast<int>(K),
-                                    static_cast<__nv_bfloat16*>(out), s);
+                                    at<int>(workspace, L.inv), static_cast<int>(T), topk, static_cast<int>(K), out,
+                                    f32_out, s);
     else
         e = launch_combine(at<__nv_bfloat16>(workspace, L.y), topk_weights, at<int>(workspace, L.inv),
-                           static_cast<int>(T), topk, static_cast<int>(K), static_cast<__nv_bfloat16*>(out), s);
+                           static_cast<int>(T), topk, static_cast<int>(K), out, f32_out, s);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     mark(5, s);
     mark_done();
     g_launches = 5 + (p13.gp.ksplit > 1 ? 1 : 0);
     return WNA16_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wna16_moe_forward(const void* x, const int32_t* topk_ids, const float* topk_weights, const int32_t* w13_packed,
+                      const uint16_t* w13_scales, const int32_t* w2_packed, const uint16_t* w2_scales, int64_t T,
+                      int64_t K, int64_t N, int64_t E, int topk, int group_size, int group_size_w2, int bits,
+                      float swiglu_limit, void* out, void* workspace, size_t workspace_bytes, void* stream) {
+    if (topk > E) {
+        g_err[0] = 0;
+        return fail(WNA16_ERR_INVALID_ARG, "topk=%d exceeds E=%lld", topk, (long long)E);
+    }
+    return forward_impl(x, topk_ids, topk_weights, w13_packed, w13_scales, w2_packed, w2_scales, T, K, N, E, 0, E,
+                        topk, group_size, group_size_w2, bits, swiglu_limit, out, false, workspace, workspace_bytes,
+                        stream);
+}
+
+int wna16_moe_forward_partial(const void* x, const int32_t* topk_ids, const float* topk_weights,
+                              const int32_t* w13_packed, const uint16_t* w13_scales, const int32_t* w2_packed,
+                              const uint16_t* w2_scales, int64_t T, int64_t K, int64_t N, int64_t E_total,
+                              int64_t expert_begin, int64_t E_local, int topk, int group_size, int group_size_w2,
+                              int bits, float swiglu_limit, float* out_partial, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    return forward_impl(x, topk_ids, topk_weights, w13_packed, w13_scales, w2_packed, w2_scales, T, K, N, E_local,
+                        expert_begin, E_total, topk, group_size, group_size_w2, bits, swiglu_limit, out_partial, true,
+                        workspace, workspace_bytes, stream);
 }
 
 int wna16_moe_route_topk(const float* logits, const float* bias, int64_t T, int64_t E, int topk, int32_t* topk_ids,
@@ -712,7 +758,7 @@ int wna16_moe_combine(const void* y, const float* topk_weights, int64_t T, int64
     const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaError_t e = launch_combine(static_cast<const __nv_bfloat16*>(y), topk_weights, at<int>(workspace, L.inv),
-                                   static_cast<int>(T), topk, static_cast<int>(K), static_cast<__nv_bfloat16*>(out),
+                                   static_cast<int>(T), topk, static_cast<int>(K), out, false,
                                    static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "combine kernel launch");
 }

@@ -63,8 +63,11 @@ int set_error(int code, const char* fmt, ...);
 cudaError_t ensure_dynamic_smem(const void* fn, int bytes);
 
 // Routing / gather / combine / pack kernels (kernels.cu).
-cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm,
-                         int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream);
+// Routing lists of the local experts [e_begin, e_begin + E) among E_total
+// (e_begin = 0, E_total = E on a single device).
+cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int* counts,
+                         int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles, int* status,
+                         cudaStream_t stream);
 // Router: ids/weights [T, k] from fp32 logits [T, E] (+ bias [E] or null);
 // 1 <= k <= min(E, 32), E <= 1024.
 cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
@@ -77,8 +80,9 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* of
 // (0, 8, 1, 9, ..., 7, 15) (or back, with inverse = 1).
 cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
                                    __nv_bfloat16* dst, cudaStream_t stream);
+// out bf16 [T, K], or with f32_out the unrounded fp32 sums (partial output)
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
-                           __nv_bfloat16* out, cudaStream_t stream);
+                           void* out, bool f32_out, cudaStream_t stream);
 // Split-K epilogues (partial sums [ksplit][mt][R][256] fp32, rows < offsets_end):
 //   h[r, n] = bf16(swiglu(sum_s gate, sum_s up)) (column n at its interleaved position if `interleave`),
 //   and with csum the offset-code corrections of h for w2 (group 128), csum[g * R + r]
@@ -89,7 +93,7 @@ cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const in
                                __nv_bfloat16* y, cudaStream_t stream);
 //   out[t, m] = bf16( sum_j w[t, j] * bf16(sum_s partial[s][m/256][inv[t, j]][m%256]) )
 cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
-                                    int T, int topk, int K, __nv_bfloat16* out, cudaStream_t stream);
+                                    int T, int topk, int K, void* out, bool f32_out, cudaStream_t stream);
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
                         cudaStream_t stream);
 // One bounded mbarrier wait that nothing completes (device failure-detection check).

@@ -58,15 +58,29 @@ __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int& ea, int
     total_b = scratch[63];
 }
 
+// Expert of slot id `g` among the local experts [e_begin, e_begin + E): its
+// local index, or -1 when it belongs to another range (skipped) or is not a
+// valid expert id at all (`bad`).
+__device__ __forceinline__ int local_expert(int g, int e_begin, int E, int E_total, bool& bad) {
+    if (g < 0 || g >= E_total) {
+        bad = true;
+        return -1;
+    }
+    const int e = g - e_begin;
+    return (e >= 0 && e < E) ? e : -1;
+}
+
 // One CTA.  Slot f = t*topk + j.  Each warp owns a contiguous run of slots;
 // pass 1 counts its slots per expert (warp-match groups), a scan over warps and
 // over experts turns the counts into start positions, pass 2 places each slot
 // (stable: ascending slot within an expert) and records the inverse map.
 // Also emits the token-tile list {expert, first row, rows} in expert order.
+// Only the experts [e_begin, e_begin + E) of the E_total are routed here
+// (all of them on a single device); slots of the other experts get inv = -1.
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    route_kernel(const int32_t* __restrict__ ids, int R, int E, int nt, int* __restrict__ counts,
-                 int* __restrict__ offsets, int* __restrict__ perm, int* __restrict__ inv, int4* __restrict__ tiles,
-                 int* __restrict__ n_tiles, int* __restrict__ status) {
+    route_kernel(const int32_t* __restrict__ ids, int R, int E, int e_begin, int E_total, int nt,
+                 int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm, int* __restrict__ inv,
+                 int4* __restrict__ tiles, int* __restrict__ n_tiles, int* __restrict__ status) {
     extern __shared__ int sm[];
     int* cnt = sm;                          // [kRouteWarps][E]
     int* scratch = sm + kRouteWarps * E;    // 64 ints
@@ -89,13 +103,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     for (int base = f0; base < f1; base += 32) {
         const int f = base + lane;
         int e = -1;
-        if (f < f1) {
-            e = ids[f];
-            if (e < 0 || e >= E) {
-                bad = true;
-                e = -1;
-            }
-        }
+        if (f < f1) e = local_expert(ids[f], e_begin, E, E_total, bad);
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
         __syncwarp();
@@ -130,10 +138,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     for (int base = f0; base < f1; base += 32) {
         const int f = base + lane;
         int e = -1;
-        if (f < f1) {
-            e = ids[f];
-            if (e < 0 || e >= E) e = -1;
-        }
+        bool ignored = false;
+        if (f < f1) e = local_expert(ids[f], e_begin, E, E_total, ignored);
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         const int pos = e >= 0 ? my[e] + __popc(peers & lt) : -1;
         __syncwarp();
@@ -311,9 +317,12 @@ __global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t bl
 }
 
 // out[t, m] = bf16( sum_j w[t, j] * y[inv[t*topk + j], m] ), fp32, j ascending;
-// a slot whose inverse index is -1 (bad expert id) adds nothing.
+// a slot whose inverse index is -1 (bad expert id, or an expert of another
+// range) adds nothing.  With F32OUT the fp32 sum is stored unrounded (the
+// partial output of an expert range).
+template <bool F32OUT>
 __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restrict__ w, const int* __restrict__ inv,
-                               int topk, int vec_per_row, uint4* __restrict__ out) {
+                               int topk, int vec_per_row, void* __restrict__ out) {
     pdl_wait();
     const int t = blockIdx.x;
     const int v = blockIdx.y * blockDim.x + threadIdx.x;
@@ -332,11 +341,17 @@ __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restr
             acc[2 * i + 1] = __fmaf_rn(wj, f.y, acc[2 * i + 1]);
         }
     }
-    uint4 o;
-    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+    if constexpr (F32OUT) {
+        float4* o = reinterpret_cast<float4*>(out) + (static_cast<int64_t>(t) * vec_per_row + v) * 2;
+        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+        uint4 o;
+        __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
-    out[static_cast<int64_t>(t) * vec_per_row + v] = o;
+        for (int i = 0; i < 4; ++i) ob[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+        reinterpret_cast<uint4*>(out)[static_cast<int64_t>(t) * vec_per_row + v] = o;
+    }
 }
 
 __device__ __forceinline__ float swiglu_clamped(float g, float u, float L) {
@@ -419,10 +434,9 @@ __global__ void finalize_w2_kernel(const float* __restrict__ partial, int ksplit
 // The lanes of a warp fetch up to 32 (slot row, weight) pairs at once and
 // pass them round by shuffles; the KS partial loads of a slot are issued
 // together.
-template <int KS>
+template <int KS, bool F32OUT>
 __global__ void combine_partials_kernel(const float* __restrict__ partial, int R, const float* __restrict__ w,
-                                        const int* __restrict__ inv, int topk, int K,
-                                        __nv_bfloat16* __restrict__ out) {
+                                        const int* __restrict__ inv, int topk, int K, void* __restrict__ out) {
     pdl_wait();
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31;
@@ -474,9 +488,15 @@ __global__ void combine_partials_kernel(const float* __restrict__ partial, int R
         }
     }
     if (!active) return;
-    __nv_bfloat162* o = reinterpret_cast<__nv_bfloat162*>(out + static_cast<int64_t>(t) * K + m0);
-    o[0] = __floats2bfloat162_rn(acc[0], acc[1]);
-    o[1] = __floats2bfloat162_rn(acc[2], acc[3]);
+    if constexpr (F32OUT) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + static_cast<int64_t>(t) * K + m0) =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
+    } else {
+        __nv_bfloat162* o =
+            reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out) + static_cast<int64_t>(t) * K + m0);
+        o[0] = __floats2bfloat162_rn(acc[0], acc[1]);
+        o[1] = __floats2bfloat162_rn(acc[2], acc[3]);
+    }
 }
 
 // word i <- codes [i*p, (i+1)*p): field j = (code_j + 2^(b-1)) & (2^b - 1) at bits [b*j, b*j+b).
@@ -494,13 +514,13 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t n_words, i
 
 }  // namespace
 
-cudaError_t launch_route(const int32_t* ids, int R, int E, int nt, int* counts, int* offsets, int* perm, int* inv,
-                         int4* tiles, int* n_tiles, int* status, cudaStream_t stream) {
+cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int* counts, int* offsets,
+                         int* perm, int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream) {
     const int smem = (kRouteWarps * E + 64) * static_cast<int>(sizeof(int));
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_kernel), smem);
     if (e != cudaSuccess) return e;
-    route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, nt, counts, offsets, perm, inv, tiles, n_tiles,
-                                                    status);
+    route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, e_begin, E_total, nt, counts, offsets, perm, inv,
+                                                    tiles, n_tiles, status);
     return cudaGetLastError();
 }
 
@@ -540,13 +560,16 @@ cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
-                           __nv_bfloat16* out, cudaStream_t stream) {
+                           void* out, bool f32_out, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const int vpr = K / 8;
     const int threads = 128;
     const dim3 grid(T, (vpr + threads - 1) / threads);
-    return launch_pdl(combine_kernel, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y), weights, inv,
-                      topk, vpr, reinterpret_cast<uint4*>(out));
+    if (f32_out)
+        return launch_pdl(combine_kernel<true>, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y),
+                          weights, inv, topk, vpr, out);
+    return launch_pdl(combine_kernel<false>, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y), weights,
+                      inv, topk, vpr, out);
 }
 
 cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
@@ -571,20 +594,27 @@ cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const in
     return launch_pdl(finalize_w2_kernel, dim3(R), dim3(256), 0, stream, partial, ksplit, R, offsets_end, K, y);
 }
 
-cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
-                                    int T, int topk, int K, __nv_bfloat16* out, cudaStream_t stream) {
-    if (T == 0) return cudaSuccess;
+template <bool F32OUT>
+static cudaError_t launch_combine_partials_t(const float* partial, int ksplit, int R, const float* weights,
+                                             const int* inv, int T, int topk, int K, void* out, cudaStream_t stream) {
     const int threads = 128;
     const dim3 grid(T, (K / 4 + threads - 1) / threads);
     switch (ksplit) {
-        case 2: return launch_pdl(combine_partials_kernel<2>, grid, dim3(threads), 0, stream, partial, R, weights, inv,
-                                  topk, K, out);
-        case 4: return launch_pdl(combine_partials_kernel<4>, grid, dim3(threads), 0, stream, partial, R, weights, inv,
-                                  topk, K, out);
-        case 8: return launch_pdl(combine_partials_kernel<8>, grid, dim3(threads), 0, stream, partial, R, weights, inv,
-                                  topk, K, out);
+        case 2: return launch_pdl(combine_partials_kernel<2, F32OUT>, grid, dim3(threads), 0, stream, partial, R,
+                                  weights, inv, topk, K, out);
+        case 4: return launch_pdl(combine_partials_kernel<4, F32OUT>, grid, dim3(threads), 0, stream, partial, R,
+                                  weights, inv, topk, K, out);
+        case 8: return launch_pdl(combine_partials_kernel<8, F32OUT>, grid, dim3(threads), 0, stream, partial, R,
+                                  weights, inv, topk, K, out);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
+                                    int T, int topk, int K, void* out, bool f32_out, cudaStream_t stream) {
+    if (T == 0) return cudaSuccess;
+    return f32_out ? launch_combine_partials_t<true>(partial, ksplit, R, weights, inv, T, topk, K, out, stream)
+                   : launch_combine_partials_t<false>(partial, ksplit, R, weights, inv, T, topk, K, out, stream);
 }
 
 // One bounded pipeline wait on a barrier that nothing completes: the wait
