@@ -101,8 +101,12 @@ WNA16_API size_t wna16_moe_workspace_size(int64_t T, int64_t K, int64_t N, int64
  *                  sizes" of page "Incubate DeepSeek V4 WNA16 runtime on SM86",
  *                  section "Validation completed"
  *   swiglu_limit   L > 0 (may be +inf)
- * Supported: bits in {2,4}; group sizes multiples of 64 that divide the
- * reduction dim (K for w13, N for w2) with at most 64 groups per row;
+ * Supported: bits in {2,4}; group sizes 32 or multiples of 64 that divide
+ * the reduction dim (K for w13, N for w2) -- a group equal to the reduction
+ * dim is one scale per output channel -- as long as the scales of one work
+ * item (256 weight rows x its groups, double-buffered) leave room for two
+ * pipeline stages in shared memory (WNA16_ERR_UNSUPPORTED otherwise; group 32
+ * fits up to a reduction dim of 4096);
  * K % 256 == 0; N % 128 == 0; 1 <= topk <= E <= 1024; T*topk < 2^31.
  * x, out, weights and scales 16-byte aligned; out must not overlap x.
  * Returns WNA16_OK or an error (nothing launched). */

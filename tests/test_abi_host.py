@@ -44,8 +44,9 @@ def _fwd(lib, *, x=A16, out=ctypes.c_void_p(0x90000), T=4, K=4096, N=2048, E=256
     (dict(bits=8), binding.ERR_UNSUPPORTED),
     (dict(K=100), binding.ERR_UNSUPPORTED),
     (dict(N=96), binding.ERR_UNSUPPORTED),
-    (dict(g=32), binding.ERR_UNSUPPORTED),
+    (dict(g=16), binding.ERR_UNSUPPORTED),
     (dict(g=96), binding.ERR_UNSUPPORTED),
+    (dict(g=48), binding.ERR_UNSUPPORTED),
     (dict(g2=192), binding.ERR_UNSUPPORTED),
     (dict(topk=9, E=8), binding.ERR_INVALID_ARG),
     (dict(E=2048), binding.ERR_UNSUPPORTED),
@@ -106,7 +107,7 @@ def test_pack_rejects_on_host(lib):
 def test_stage_entry_points_reject_on_host(lib):
     assert lib.wna16_moe_route(A16, 4, 8, 256, 4096, 2048, 3, None, None, None, None, A16, 1 << 40,
                                None) == binding.ERR_UNSUPPORTED
-    assert lib.wna16_moe_w13(A16, A16, A16, A16, 4, 4096, 2048, 256, 8, 32, 2, 7.0, A16, A16, 1 << 40,
+    assert lib.wna16_moe_w13(A16, A16, A16, A16, 4, 4096, 2048, 256, 8, 16, 2, 7.0, A16, A16, 1 << 40,
                              None) == binding.ERR_UNSUPPORTED
     assert lib.wna16_moe_w2(A16, A16, A16, 4, 4096, 2048, 256, 8, 128, 2, A16, A16, 16, None) == \
         binding.ERR_WORKSPACE_TOO_SMALL

@@ -277,6 +277,30 @@ def test_plan_threshold_matrix(moe, oracle, rows, bits, g13, g2):
     _check_all_tokens(moe, oracle, w, inp, f"rows={rows} bits={bits} g={g13}/{g2}")
 
 
+@pytest.mark.parametrize("rows", [1, 16, 17, 129])
+@pytest.mark.parametrize("bits,g13,g2", [(2, 32, 32), (4, 32, 128), (2, 1024, 512), (4, 1024, 512)],
+                         ids=["w2-g32", "w4-g32/g128", "w2-per-channel", "w4-per-channel"])
+def test_group_32_and_per_channel(moe, oracle, rows, bits, g13, g2):
+    """Group 32 (two scales in every 64-k dequant chunk) and one scale per
+    output channel (group = the reduction dim: 1024 for w13, 512 for w2),
+    across token-tile and split-K plans."""
+    E, topk = 8, 2
+    w = _small(T=E * rows // topk, K=1024, N=512, E=E, topk=topk, bits=bits, g13=g13, g2=g2)
+    inp = _inputs(w)
+    inp["ids"] = _exact_rows_ids(E, topk, rows)
+    _check_all_tokens(moe, oracle, w, inp, f"rows={rows} bits={bits} g={g13}/{g2}")
+
+
+@pytest.mark.parametrize("bits,T", [(2, 4), (4, 4), (2, 512), (4, 512)])
+def test_group_32_full_hidden(moe, oracle, bits, T):
+    """Group 32 at hidden 4096 / intermediate 2048: decode (4 tokens over 256
+    experts, split K) and prefill-sized tiles (512 tokens over 8 experts, 128
+    scale groups of w13 per work item in shared memory)."""
+    E = 256 if T == 4 else 8
+    w = _small(T=T, K=4096, N=2048, E=E, topk=8 if T == 4 else 2, bits=bits, g13=32, g2=32)
+    _check_all_tokens(moe, oracle, w, _inputs(w), f"g32 full hidden bits={bits} T={T}")
+
+
 # ---------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("bits", [4, 2])

@@ -110,10 +110,10 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.max_tiles = (L.R < E ? L.R : E) + L.R / L.nt + 1;
     L.units13 = L.max_tiles * (N / 128);
     L.units2 = L.max_tiles * (K / 256);
-    // split-K partial sums for the largest split any group size could give (64
+    // split-K partial sums for the largest split any group size could give (32
     // is the smallest supported group): splits x row tiles x R token rows x 256
-    const int64_t s13 = choose_split(L.units13, K, stage_k(L.nt, bits, K), 64);
-    const int64_t s2 = choose_split(L.units2, N, stage_k(L.nt, bits, N), 64);
+    const int64_t s13 = choose_split(L.units13, K, stage_k(L.nt, bits, K), 32);
+    const int64_t s2 = choose_split(L.units2, N, stage_k(L.nt, bits, N), 32);
     const int64_t p13 = s13 > 1 ? s13 * (N / 128) * L.R * 256 : 0;
     const int64_t p2 = s2 > 1 ? s2 * (K / 256) * L.R * 256 : 0;
     const int64_t partial_floats = p13 > p2 ? p13 : p2;
@@ -255,11 +255,13 @@ int check_dims(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bits) {
     return WNA16_OK;
 }
 
+// Group sizes: 32, or multiples of 64 (up to the whole reduction dim: one
+// scale per output channel), dividing the reduction dim.  Whether the scales
+// of one work item fit in shared memory is checked when the launch is planned.
 int check_group(int g, int64_t kred, const char* name) {
-    if (g <= 0 || g % 64 || kred % g)
-        return fail(WNA16_ERR_UNSUPPORTED, "%s=%d: groups must be multiples of 64 that divide %lld", name, g,
+    if (g <= 0 || (g != 32 && g % 64) || kred % g)
+        return fail(WNA16_ERR_UNSUPPORTED, "%s=%d: groups must be 32 or multiples of 64 that divide %lld", name, g,
                     (long long)kred);
-    if (kred / g > 64) return fail(WNA16_ERR_UNSUPPORTED, "%s=%d: at most 64 groups per row", name, g);
     return WNA16_OK;
 }
 
@@ -313,8 +315,11 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     const int64_t max_units = w13 ? L.units13 : L.units2;
     const int ksplit = choose_split(max_units, kred, kp, group);
     const int ngroups = static_cast<int>(kred / group);
-    GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups, dev.max_smem);
-    if (sm.nstage < 2) return fail(WNA16_ERR_UNSUPPORTED, "shared-memory plan does not fit");
+    GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups / ksplit, dev.max_smem);
+    if (sm.nstage < 2)
+        return fail(WNA16_ERR_UNSUPPORTED,
+                    "shared-memory plan does not fit (%d scale groups per work item of 256 rows; group %d along %lld)",
+                    ngroups / ksplit, group, (long long)kred);
 
     const int p = 32 / bits;
     {

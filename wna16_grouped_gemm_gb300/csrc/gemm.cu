@@ -274,6 +274,36 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t* row, uint32_t xr, i
     }
 }
 
+// Group 32: the first 32 k of a 64-k half take scale s_a, the second s_b
+// (same layout and exact rounding as dequant_chunk).
+template <int BITS>
+__device__ __forceinline__ void dequant_chunk_g32(const uint8_t* row, uint32_t xr, int chunk, float s_a, float s_b,
+                                                  uint32_t (&o)[32]) {
+    if constexpr (BITS == 2) {
+        // words of 16 k: x, y in the first 32 k, z, w in the second
+        const uint4 v = *reinterpret_cast<const uint4*>(row + ((static_cast<uint32_t>(chunk) ^ xr) << 4));
+        const Scale2 ca(s_a), cb(s_b);
+        dequant_word2_pairs(v.x, ca, o + 0);
+        dequant_word2_pairs(v.y, ca, o + 8);
+        dequant_word2_pairs(v.z, cb, o + 16);
+        dequant_word2_pairs(v.w, cb, o + 24);
+    } else {
+        // 16-byte vectors of 32 k: v0 the first 32 k, v1 the second
+        const uint32_t j0 = static_cast<uint32_t>(2 * chunk);
+        const uint4 v0 = *reinterpret_cast<const uint4*>(row + ((j0 ^ xr) << 4));
+        const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((j0 + 1) ^ xr) << 4));
+        const Neg4 ca(s_a), cb(s_b);
+        dequant_word4(v0.x, s_a, ca, o + 0);
+        dequant_word4(v0.y, s_a, ca, o + 4);
+        dequant_word4(v0.z, s_a, ca, o + 8);
+        dequant_word4(v0.w, s_a, ca, o + 12);
+        dequant_word4(v1.x, s_b, cb, o + 16);
+        dequant_word4(v1.y, s_b, cb, o + 20);
+        dequant_word4(v1.z, s_b, cb, o + 24);
+        dequant_word4(v1.w, s_b, cb, o + 28);
+    }
+}
+
 __device__ __forceinline__ float swiglu(float g, float u, float L) {
     g = fminf(g, L);
     u = fminf(fmaxf(u, -L), L);
@@ -602,7 +632,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
             int r0, r1;
             unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
             // buffer layout [256 rows][ng_item] fp16
-            uint8_t* dst = reinterpret_cast<uint8_t*>(sS + sb.idx * (ng * 2 * kRowsPerTile));
+            uint8_t* dst = reinterpret_cast<uint8_t*>(sS + sb.idx * (ng_item * 2 * kRowsPerTile));
             if (cb) {
                 const int cpr = rb / cb;           // copies per row
                 for (int i = lane; i < 2 * kRowsPerTile * cpr; i += 32) {
@@ -641,19 +671,31 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
         const uint32_t abase = tmem + abase_col + lane_base + static_cast<uint32_t>(blk * 64);
         Ring st, ab, sb;
         bool ok = true;
-        const int halves_per_group = p.group / 64;
+        const bool g32 = p.group == 32;
+        const int halves_per_group = g32 ? 1 : p.group / 64;
         for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
             const int u = v / ksplit;
             const int split = v - u * ksplit;
             // GA mode: the epilogue warps apply the scales, not these warps
             if (!ga && !mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
-            const uint16_t* srow = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + (blk * kRowsPerTile + row) * ng_item;
-            int gi = 0, gleft = halves_per_group;   // scale group of the current 64-k half
+            const uint16_t* srow = sS + sb.idx * (ng_item * 2 * kRowsPerTile) + (blk * kRowsPerTile + row) * ng_item;
+            // scale group of the current 64-k half (group 32: the first of its two groups)
+            int gi = 0, gleft = halves_per_group;
             auto next_half = [&]() {
-                if (--gleft == 0) {
+                if (g32) {
+                    gi += 2;
+                } else if (--gleft == 0) {
                     gleft = halves_per_group;
                     ++gi;
                 }
+            };
+            // one 64-k half of weights: one scale, or (group 32) one per 32 k
+            auto half_chunk = [&](const uint8_t* wr, int chunk, uint32_t (&v)[32]) {
+                if (g32)
+                    dequant_chunk_g32<BITS>(wr, xr, chunk, __half2float(__ushort_as_half(srow[gi])),
+                                            __half2float(__ushort_as_half(srow[gi + 1])), v);
+                else
+                    dequant_chunk<BITS>(wr, xr, chunk, __half2float(__ushort_as_half(srow[gi])), v);
             };
             for (int ks = split * kps; ks < (split + 1) * kps && ok; ++ks) {
                 if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
@@ -678,10 +720,10 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                         } else if (ga) {
                             codes_chunk2<false>(wrow, xr, 2 * c, v32);
                         } else {
-                            dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[gi])), v32);
+                            half_chunk(wrow, 2 * c, v32);
                         }
                     } else {
-                        dequant_chunk<BITS>(wrow, xr, 2 * c, __half2float(__ushort_as_half(srow[gi])), v32);
+                        half_chunk(wrow, 2 * c, v32);
                     }
                     next_half();
                     if (!a_ready && !mbar_wait_bounded(&aempty[abar], ab.phase ^ 1u, abort_flag, status)) {
@@ -696,10 +738,10 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                         } else if (ga) {
                             codes_chunk2<false>(wrow, xr, 2 * c + 1, v32);
                         } else {
-                            dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[gi])), v32);
+                            half_chunk(wrow, 2 * c + 1, v32);
                         }
                     } else {
-                        dequant_chunk<BITS>(wrow, xr, 2 * c + 1, __half2float(__ushort_as_half(srow[gi])), v32);
+                        half_chunk(wrow, 2 * c + 1, v32);
                     }
                     next_half();
                     tc_st_32x32b_x32(abase + ab.idx * 128 + 32, v32);
@@ -848,7 +890,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     const int split = v - u * ksplit;
                     const int4 tile = p.tiles[u / p.mt_count];
                     if (!mbar_wait_bounded(&sfull[sb.idx], sb.phase, abort_flag, status)) break;
-                    const uint16_t* s0row = sS + sb.idx * (p.ngroups * 2 * kRowsPerTile) + row * ng_item;
+                    const uint16_t* s0row = sS + sb.idx * (ng_item * 2 * kRowsPerTile) + row * ng_item;
                     const uint16_t* s1row = s0row + kRowsPerTile * ng_item;
                     // corrections of this item's groups for the tile's token rows
                     const float* crow = goff ? p.csum + static_cast<int64_t>(split * ng_item) * R_rows + tile.y : nullptr;
@@ -996,12 +1038,12 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem) {
+GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ng_item, int max_smem) {
     GemmSmem L{};
     const int pitch = kp * bits / 8;
     const int b_stage = (kp / 64) * nt * 128;
     const int w_stage = 2 * kRowsPerTile * pitch;
-    const int s_bytes = 2 * ngroups * 2 * kRowsPerTile * 2;
+    const int s_bytes = 2 * ng_item * 2 * kRowsPerTile * 2;   // two item buffers [256 rows][ng_item] fp16
     const int bar_bytes = 8 * (2 * 16 + 4 * kMaxABuf + 4 + 4 + kMaxIssuers + 2 * kGaSlots) + 16;
     const int fixed = s_bytes + bar_bytes + 1024 /*alignment slack*/;
     int ns = (max_smem - fixed) / (b_stage + w_stage);

@@ -18,7 +18,7 @@ struct GemmParams {
     int half_rows;              // N (w13: first up row)
     int kred;                   // reduction length: K (w13) or N (w2)
     int ngroups;                // kred / group
-    int group;                  // scale group along the reduction dim
+    int group;                  // scale group along the reduction dim (32, or a multiple of 64)
     int mt_count;               // 256-row units per expert: N/128 (w13) or K/256 (w2)
     int kp;                     // K elements per pipeline stage
     int nt;                     // token tile (MMA N): 16, 32, 64 or 128
@@ -48,8 +48,9 @@ struct GemmSmem {
     int total = 0;
 };
 
-// Shared-memory plan for one launch; nstage < 2 means it does not fit.
-GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ngroups, int max_smem);
+// Shared-memory plan for one launch (ng_item = scale groups per work item);
+// nstage < 2 means it does not fit.
+GemmSmem gemm_smem_layout(int bits, int nt, int kp, int ng_item, int max_smem);
 
 cudaError_t launch_grouped_gemm(int bits, bool w13, const CUtensorMap& tm_w, const CUtensorMap& tm_b,
                                 const GemmParams& p, int grid, int smem_bytes, cudaStream_t stream);
