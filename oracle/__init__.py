@@ -36,6 +36,8 @@ MUTATIONS = {
     "topk_tie_high": 10,
     "topk_no_renorm": 11,
     "topk_no_bias": 12,
+    "q_no_importance": 13,
+    "q_clamp_high": 14,
 }
 
 
@@ -82,6 +84,10 @@ def _load():
     lib.oracle_combine_partial.restype = I
     lib.oracle_sum_partials.argtypes = [P, I, I64, P]
     lib.oracle_sum_partials.restype = I
+    lib.oracle_fp16_rne.argtypes = [ctypes.c_double]
+    lib.oracle_fp16_rne.restype = ctypes.c_uint16
+    lib.oracle_quantize.argtypes = [P, I64, I64, P, I, I64, I, P, P, P]
+    lib.oracle_quantize.restype = I
     lib.oracle_route_topk.argtypes = [P, P, I64, I64, I, P, P]
     lib.oracle_route_topk.restype = I
     lib.oracle_num_threads.argtypes = []
@@ -124,6 +130,11 @@ def bf16_to_double(b: int) -> float:
 def bf16_rne(v: float) -> int:
     """Nearest bfloat16 (ties to even) of a double, as its 16-bit pattern."""
     return int(_load().oracle_bf16_rne(float(v)))
+
+
+def fp16_rne(v: float) -> int:
+    """Nearest binary16 (ties to even) of a double, as its 16-bit pattern."""
+    return int(_load().oracle_fp16_rne(float(v)))
 
 
 def pack(codes: np.ndarray, bits: int) -> np.ndarray:
@@ -256,3 +267,22 @@ def sum_partials(partials) -> np.ndarray:
     if _load().oracle_sum_partials(_ptr(p), P, int(np.prod(p.shape[1:])), _ptr(out)) != 0:
         raise OracleError("sum_partials: bad arguments")
     return out
+
+
+def quantize(w: np.ndarray, bits: int, group: int, importance: np.ndarray | None = None, search: bool = True):
+    """Symmetric RTN quantiser with an importance-weighted scale search (the
+    definition in wna16_oracle.c).  w fp32 [rows, K], importance fp32 [K] or
+    None; returns (packed int32 [rows, K*bits/32], scales fp16 [rows, K/group],
+    metrics fp64 [rows, 4]: weighted error, unweighted error, sum a w^2, sum w^2)."""
+    wa = _c(w, np.float32)
+    rows, K = wa.shape
+    imp = None if importance is None else _c(importance, np.float32)
+    if imp is not None and imp.shape != (K,):
+        raise OracleError("importance must be [K]")
+    packed = np.empty((rows, K * bits // 32), np.int32)
+    scales = np.empty((rows, K // group), np.uint16)
+    metrics = np.empty((rows, 4), np.float64)
+    if _load().oracle_quantize(_ptr(wa), rows, K, _ptr(imp), bits, group, 1 if search else 0, _ptr(packed),
+                               _ptr(scales), _ptr(metrics)) != 0:
+        raise OracleError("quantize: bad arguments")
+    return packed, scales.view(np.float16), metrics

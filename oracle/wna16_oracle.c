@@ -67,7 +67,9 @@ enum {
     MUT_TOPK_TIE_HIGH = 10, /* router: equal scores go to the higher index       */
     MUT_TOPK_NO_RENORM = 11,/* router: weights left as full-softmax probabilities */
     MUT_TOPK_NO_BIAS = 12,  /* router: the bias is ignored                       */
-    MUT_LAST = 13
+    MUT_Q_NO_IMPORTANCE = 13,/* quantiser: the importance weights are ignored     */
+    MUT_Q_CLAMP_HIGH = 14,  /* quantiser: codes clamped to 2^(b-1) (one too far) */
+    MUT_LAST = 15
 };
 static int g_mutation = MUT_NONE;
 
@@ -449,6 +451,151 @@ int oracle_forward(const uint16_t* x, const int32_t* ids, const float* wts,
         for (int64_t q = 0; q < R * K; ++q) y_out[q] = oracle_bf16_rne(ybuf[q]);
 
     free(W13); free(W2); free(hbuf); free(ybuf); free(xrow);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* Quantiser: symmetric RTN with an importance-weighted scale search.    */
+/* ------------------------------------------------------------------ */
+
+/* binary16 bit pattern of the nearest fp16 to a double, ties to even (one
+ * rounding; overflow to infinity). */
+uint16_t oracle_fp16_rne(double v)
+{
+    if (isnan(v)) return 0x7e00;
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);                       /* a = m * 2^e, m in [0.5, 1) */
+    int q = e - 11;                     /* quantum of an 11-bit significand */
+    if (q < -24) q = -24;               /* subnormal quantum */
+    double n = nearbyint(ldexp(a, -q));
+    double r = ldexp(n, q);
+    if (r >= 65520.0) return sign | 0x7c00;   /* beyond the largest finite half (65504) after rounding */
+    if (r < ldexp(1.0, -14))                   /* subnormal: mantissa = r / 2^-24 */
+        return sign | (uint16_t)(r * 16777216.0);
+    int ee;
+    double m = frexp(r, &ee);           /* r = m * 2^ee, m in [0.5, 1) */
+    uint16_t man = (uint16_t)(ldexp(m, 11) - 1024.0);
+    return sign | (uint16_t)((ee + 14) << 10) | man;
+}
+
+/*
+ * The quantiser that produces the packed words and FP16 scales the forward
+ * consumes, following the conversion the weight-format page describes
+ * ("hampsonw/DeepSeek-V4-Flash-0731-WNA16", section "How it was created":
+ * symmetric b-bit weights fitted with group size 128 (step 2), the scale
+ * search weighted by a routed-expert activation importance vector (step 3),
+ * signed codes packed (step 4), weighted and unweighted reconstruction error
+ * recorded (step 5); "imatrix-weighted RTN").  Per row and group of g
+ * consecutive k, with lo = -2^(b-1), hi = 2^(b-1) - 1:
+ *
+ *   m      = max |w_k|
+ *   s0     = m / 2^(b-1)                 the largest magnitude lands on lo
+ *   cand i = fp16( fp32(s0 * f_i) ),  f_i = fp32((10 + i) / 20), i = 0..30
+ *            (f from 0.5 to 2.0 in steps of 0.05; f_10 = 1 is plain RTN);
+ *            search = 0 tries f_10 only
+ *   code_k = clamp( rne( fp32(w_k / s) ), lo, hi )     for a candidate s
+ *   what_k = bf16( code_k * s )                        the forward's dequantisation
+ *   E(s)   = sum_k a_k (w_k - what_k)^2    fp64, k ascending (a = 1 without importance)
+ *   chosen = the candidate of smallest E; ties to the lower i
+ *
+ * A group whose largest magnitude is 0 gets scale 0 and codes 0.  The codes
+ * and the candidate are integer decisions taken on fp32 divisions and fp64
+ * sums that the kernel performs in the same precision and order.
+ *
+ * w fp32 [rows, K]; importance fp32 [K] or NULL; packed int32 [rows, K/p];
+ * scales fp16 bits [rows, K/g]; metrics fp64 [rows, 4] or NULL: per row, in
+ * group order, sum a (w - what)^2, sum (w - what)^2, sum a w^2, sum w^2.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_quantize(const float* w, int64_t rows, int64_t K, const float* importance, int bits, int64_t g,
+                    int search, int32_t* packed, uint16_t* scales, double* metrics)
+{
+    if ((bits != 2 && bits != 4) || g <= 0 || K % g || g % codes_per_word(bits) || rows < 0) return -1;
+    const int p = codes_per_word(bits);
+    const int lo = -(1 << (bits - 1));
+    const int hi = (1 << (bits - 1)) - 1 + (g_mutation == MUT_Q_CLAMP_HIGH ? 1 : 0);
+    const int64_t groups = K / g;
+    int8_t* codes = (int8_t*)malloc((size_t)K);
+    if (!codes) return -1;
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* wr = w + r * K;
+        double row_ew = 0.0, row_eu = 0.0, row_aw = 0.0, row_w = 0.0;
+        for (int64_t gi = 0; gi < groups; ++gi) {
+            const float* wg = wr + gi * g;
+            float m = 0.0f;
+            for (int64_t k = 0; k < g; ++k) {
+                float a = fabsf(wg[k]);
+                if (a > m) m = a;
+            }
+            float best_s = 0.0f;
+            if (m > 0.0f) {
+                const float s0 = m / (float)(1 << (bits - 1));
+                double best_e = 0.0;
+                int first = 1;
+                for (int i = 0; i <= 30; ++i) {
+                    if (!search && i != 10) continue;
+                    const float f = (float)(10 + i) / 20.0f;
+                    const float prod = s0 * f;
+                    const uint16_t sh = oracle_fp16_rne((double)prod);
+                    const float s = (float)oracle_fp16_to_double(sh);
+                    if (!(s > 0.0f) || isinf(s)) continue;
+                    double e = 0.0;
+                    for (int64_t k = 0; k < g; ++k) {
+                        float qf = nearbyintf(wg[k] / s);
+                        if (qf < (float)lo) qf = (float)lo;
+                        if (qf > (float)hi) qf = (float)hi;
+                        const double what = oracle_bf16_to_double(oracle_bf16_rne((double)qf * (double)s));
+                        const double d = (double)wg[k] - what;
+                        const double a = (importance && g_mutation != MUT_Q_NO_IMPORTANCE)
+                                             ? (double)importance[gi * g + k] : 1.0;
+                        e = e + (a * d) * d;
+                    }
+                    if (first || e < best_e) {
+                        best_e = e;
+                        best_s = s;
+                        first = 0;
+                    }
+                }
+            }
+            scales[r * groups + gi] = oracle_fp16_rne((double)best_s);
+            /* codes, reconstruction and the row's metrics for the chosen scale */
+            for (int64_t k = 0; k < g; ++k) {
+                int c = 0;
+                double what = 0.0;
+                if (best_s > 0.0f) {
+                    float qf = nearbyintf(wg[k] / best_s);
+                    if (qf < (float)lo) qf = (float)lo;
+                    if (qf > (float)hi) qf = (float)hi;
+                    c = (int)qf;
+                    what = oracle_bf16_to_double(oracle_bf16_rne((double)qf * (double)best_s));
+                }
+                codes[gi * g + k] = (int8_t)c;
+                const double d = (double)wg[k] - what;
+                const double a = importance ? (double)importance[gi * g + k] : 1.0;
+                row_ew = row_ew + (a * d) * d;
+                row_eu = row_eu + d * d;
+                row_aw = row_aw + (a * (double)wg[k]) * (double)wg[k];
+                row_w = row_w + (double)wg[k] * (double)wg[k];
+            }
+        }
+        /* pack: field j of word i holds code p*i + j + 2^(b-1) at bits [b*j, b*j + b) */
+        for (int64_t wi = 0; wi < K / p; ++wi) {
+            uint32_t word = 0;
+            for (int j = 0; j < p; ++j)
+                word |= ((uint32_t)(codes[wi * p + j] - lo) & ((1u << bits) - 1u)) << (bits * j);
+            packed[r * (K / p) + wi] = (int32_t)word;
+        }
+        if (metrics) {
+            metrics[r * 4 + 0] = row_ew;
+            metrics[r * 4 + 1] = row_eu;
+            metrics[r * 4 + 2] = row_aw;
+            metrics[r * 4 + 3] = row_w;
+        }
+    }
+    free(codes);
     return 0;
 }
 

@@ -398,10 +398,95 @@ def pin_ep_profile(oracle):
     assert np.all(oracle.sum_partials([p, -p]) == 0)
 
 
+def pin_fp16_rounding(oracle):
+    """One-step RNE to binary16 equals numpy's double -> half conversion."""
+    rng = np.random.default_rng(31)
+    vals = list(rng.standard_normal(400) * np.exp(rng.uniform(-20, 12, 400)))
+    vals += [65504.0, 65519.99, 65520.0, 70000.0, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26, 2.0 ** -14,
+             (2.0 ** -14) * (1 - 2.0 ** -12), 1 + 2.0 ** -11, 1 + 3 * 2.0 ** -11, -0.0, 0.0]
+    with np.errstate(over="ignore"):
+        for v in vals:
+            assert oracle.fp16_rne(v) == int(np.array(v, np.float64).astype(np.float16).view(np.uint16)), v
+
+
+def _q_case(rows=6, K=256, seed=41, scale=0.02):
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((rows, K)) * scale).astype(np.float32)
+    w[:, 5] *= 6.0                     # an outlier column
+    imp = np.exp(rng.standard_normal(K)).astype(np.float32)
+    return w, imp
+
+
+def pin_quantizer(oracle):
+    """Quantiser: weights that are exactly code x scale come back exactly;
+    the searched scale never has a larger weighted error than plain RTN (f = 1
+    is a candidate); the packed words and scales, dequantised by the forward's
+    own dequantisation, reproduce the reconstruction the errors were measured
+    on; scaling w by 8 scales the scales by 8 and the errors by 64 exactly;
+    a one-hot importance picks the candidate best for that one weight (checked
+    in exact rational arithmetic over all 31 candidates); an all-zero group
+    gets scale 0 and code 0."""
+    from fractions import Fraction
+    for bits in (2, 4):
+        lo, hi = -(1 << (bits - 1)), (1 << (bits - 1)) - 1
+        p = 32 // bits
+        rng = np.random.default_rng(bits)
+        # (a) exact representability, plain RTN
+        codes = rng.integers(lo, hi + 1, size=(3, 128)).astype(np.int8)
+        codes[:, 7] = lo
+        sv = np.array([1.25 * 2.0 ** -6, 1.5 * 2.0 ** -9, 0.375], np.float16)   # products exact in BF16
+        w = (codes.astype(np.float32) * sv.astype(np.float32)[:, None]).astype(np.float32)
+        pk, sc, m = oracle.quantize(w, bits, 128, None, search=False)
+        assert np.array_equal(sc.view(np.uint16)[:, 0], sv.view(np.uint16))
+        assert np.array_equal(oracle.unpack(pk, 128, bits), codes)
+        assert np.all(m[:, 0] == 0) and np.all(m[:, 1] == 0)
+        w, imp = _q_case()
+        for g in (32, 128):
+            pk0, sc0, m0 = oracle.quantize(w, bits, g, imp, search=False)
+            pk1, sc1, m1 = oracle.quantize(w, bits, g, imp, search=True)
+            assert np.all(m1[:, 0] <= m0[:, 0]) and m1[:, 0].sum() < m0[:, 0].sum()
+            # (c) consistency with the forward's dequantisation
+            for pk_, sc_, m_ in ((pk0, sc0, m0), (pk1, sc1, m1)):
+                deq = _bf16_to_f64(oracle.dequant(pk_, sc_, w.shape[1], g, bits))
+                d = w.astype(np.float64) - deq
+                assert np.allclose(m_[:, 1], (d * d).sum(axis=1), rtol=1e-12, atol=0)
+                assert np.allclose(m_[:, 0], (imp * d * d).sum(axis=1), rtol=1e-12, atol=0)
+                assert np.allclose(m_[:, 3], (w.astype(np.float64) ** 2).sum(axis=1), rtol=1e-12)
+            # (d) power-of-two homogeneity
+            pk8, sc8, m8 = oracle.quantize(w * np.float32(8), bits, g, imp, search=True)
+            assert np.array_equal(pk8, pk1)
+            assert np.array_equal(sc8.astype(np.float64), 8 * sc1.astype(np.float64))
+            assert np.array_equal(m8, 64 * m1)
+        # (e) one-hot importance, exact arithmetic over the candidates
+        wg = w[:1, :128]
+        k0 = 5
+        onehot = np.zeros(128, np.float32)
+        onehot[k0] = 1.0
+        _, sc, _ = oracle.quantize(wg, bits, 128, onehot, search=True)
+        mx = Fraction(float(np.abs(wg).max()))
+
+        def err(sf):
+            s = Fraction(sf)
+            q = max(lo, min(hi, round(Fraction(float(np.float32(wg[0, k0]) / np.float32(sf))))))
+            return abs(Fraction(float(wg[0, k0])) - Fraction(ind.bf16_value(ind.bf16_bits_exact(q * s))))
+        cands = []
+        for i in range(31):
+            f = np.float32(10 + i) / np.float32(20)
+            s0 = np.float32(float(mx)) / np.float32(1 << (bits - 1))
+            cands.append(float(np.float16(np.float32(s0 * f))))
+        best = min(err(c) for c in cands)
+        assert err(float(sc[0, 0])) == best, bits
+        # (g) an all-zero group
+        z = np.zeros((1, 128), np.float32)
+        pkz, scz, mz = oracle.quantize(z, bits, 128, imp[:128], search=True)
+        assert scz[0, 0] == 0 and np.all(oracle.unpack(pkz, 128, bits) == 0) and np.all(mz == 0)
+        assert p * pkz.shape[1] == 128
+
+
 PINS = [pin_fp16_decode, pin_bf16_rounding, pin_hand_words, pin_pack_roundtrip, pin_dequant,
         pin_route, pin_zero_codes, pin_brute_force, pin_dense_mlp, pin_clamp_closed_form,
         pin_scale_doubling, pin_relabel_and_token_permutation, pin_split_routing_weight, pin_fp32_mode,
-        pin_given_h, pin_router, pin_ep_profile]
+        pin_given_h, pin_router, pin_ep_profile, pin_fp16_rounding, pin_quantizer]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
