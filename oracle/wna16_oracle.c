@@ -506,8 +506,9 @@ uint16_t oracle_fp16_rne(double v)
  * sums that the kernel performs in the same precision and order.
  *
  * w fp32 [rows, K]; importance fp32 [K] or NULL; packed int32 [rows, K/p];
- * scales fp16 bits [rows, K/g]; metrics fp64 [rows, 4] or NULL: per row, in
- * group order, sum a (w - what)^2, sum (w - what)^2, sum a w^2, sum w^2.
+ * scales fp16 bits [rows, K/g]; metrics fp64 [rows, 4] or NULL: per row,
+ * sum a (w - what)^2, sum (w - what)^2, sum a w^2, sum w^2, each summed per
+ * group (k ascending, fp64) and the group sums added in group order.
  * Returns 0, or -1 on a bad argument.
  */
 int oracle_quantize(const float* w, int64_t rows, int64_t K, const float* importance, int bits, int64_t g,
@@ -561,7 +562,8 @@ int oracle_quantize(const float* w, int64_t rows, int64_t K, const float* import
                 }
             }
             scales[r * groups + gi] = oracle_fp16_rne((double)best_s);
-            /* codes, reconstruction and the row's metrics for the chosen scale */
+            /* codes, reconstruction and the group's metrics for the chosen scale */
+            double gew = 0.0, geu = 0.0, gaw = 0.0, gw = 0.0;
             for (int64_t k = 0; k < g; ++k) {
                 int c = 0;
                 double what = 0.0;
@@ -575,11 +577,15 @@ int oracle_quantize(const float* w, int64_t rows, int64_t K, const float* import
                 codes[gi * g + k] = (int8_t)c;
                 const double d = (double)wg[k] - what;
                 const double a = importance ? (double)importance[gi * g + k] : 1.0;
-                row_ew = row_ew + (a * d) * d;
-                row_eu = row_eu + d * d;
-                row_aw = row_aw + (a * (double)wg[k]) * (double)wg[k];
-                row_w = row_w + (double)wg[k] * (double)wg[k];
+                gew = gew + (a * d) * d;
+                geu = geu + d * d;
+                gaw = gaw + (a * (double)wg[k]) * (double)wg[k];
+                gw = gw + (double)wg[k] * (double)wg[k];
             }
+            row_ew = row_ew + gew;
+            row_eu = row_eu + geu;
+            row_aw = row_aw + gaw;
+            row_w = row_w + gw;
         }
         /* pack: field j of word i holds code p*i + j + 2^(b-1) at bits [b*j, b*j + b) */
         for (int64_t wi = 0; wi < K / p; ++wi) {
