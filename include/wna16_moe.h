@@ -166,6 +166,37 @@ WNA16_API int wna16_moe_read_status(const void* workspace, int* device_status, v
 WNA16_API int wna16_moe_route_topk(const float* logits, const float* bias, int64_t T, int64_t E, int topk,
                                    int32_t* topk_ids, float* topk_weights, void* stream);
 
+/* Quantiser: the conversion step that produces the packed words and FP16
+ * scales this library consumes -- symmetric RTN with an importance-weighted
+ * scale search (page "hampsonw/DeepSeek-V4-Flash-0731-WNA16", section "How it
+ * was created", steps 2-5, and its note that importance-weighted RTN was
+ * selected).  Per row and group of group_size consecutive k, with
+ * lo = -2^(bits-1), hi = 2^(bits-1) - 1:
+ *   m = max|w|, s0 = m / 2^(bits-1)
+ *   candidates s_i = fp16(fp32(s0 * fp32((10 + i) / 20))), i = 0..30 (factors
+ *     0.5 .. 2.0); search = 0: s_10 only (plain RTN)
+ *   code = clamp(round-half-even(fp32(w / s)), lo, hi); what = bf16(code * s)
+ *     (the forward's dequantisation)
+ *   E(s) = sum_k importance[k] * (w - what)^2, fp64, k ascending (importance
+ *     1 when NULL); the smallest E wins, ties to the lower i; a group of zeros
+ *     gets scale 0.
+ *   w           fp32 device [rows, K], 16-byte aligned
+ *   importance  fp32 device [K] (per input channel, >= 0) or NULL
+ *   packed      int32 device [rows, K*bits/32] (written; the format of
+ *               wna16_moe_pack)
+ *   scales      fp16 device [rows, K/group_size] (written)
+ *   metrics     fp64 device [rows, 4] or NULL (written): per row, weighted
+ *               error sum a (w - what)^2, unweighted error sum (w - what)^2,
+ *               sum a w^2 and sum w^2, each as per-group fp64 sums added in
+ *               group order
+ * group_size a multiple of 32 dividing K, K/group_size <= 128.  The result is
+ * bit-for-bit reproducible (IEEE operations in a fixed order).  Asynchronous
+ * on `stream`; returns WNA16_OK, WNA16_ERR_INVALID_ARG, WNA16_ERR_UNSUPPORTED
+ * or WNA16_ERR_CUDA. */
+WNA16_API int wna16_moe_quantize(const float* w, int64_t rows, int64_t K, const float* importance, int bits,
+                                 int group_size, int search, int32_t* packed, uint16_t* scales, double* metrics,
+                                 void* stream);
+
 /* Message for the last host-side error on the calling thread ("" if none). */
 WNA16_API const char* wna16_moe_last_error(void);
 

@@ -161,3 +161,16 @@ def random_codes(rng: np.random.Generator, shape, bits: int) -> np.ndarray:
     """Uniform signed codes in [-2^(b-1), 2^(b-1)) as int8 (for pack tests)."""
     half = 1 << (bits - 1)
     return rng.integers(-half, half, size=shape, dtype=np.int8)
+
+
+def make_quant_inputs(rows: int, K: int, seed: int = 0):
+    """Source weights for the quantiser, fp32 [rows, K]: N(0, 0.02^2) with 1 %
+    of the entries eight times larger (heavy-tailed, like decoded expert
+    weights), and an importance vector fp32 [K] (per input channel, the mean
+    squared activation of a calibration set: log-normal, exp(N(0, 1)))."""
+    rng = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 7])))
+    w = rng.standard_normal((rows, K), dtype=np.float32) * np.float32(0.02)
+    out = rng.random((rows, K)) < 0.01
+    w[out] *= np.float32(8.0)
+    imp = np.exp(rng.standard_normal(K)).astype(np.float32)
+    return w, imp

@@ -19,7 +19,7 @@ def lib():
 
 def test_every_declared_symbol_is_exported(lib):
     names = binding.exported_names_in_header()
-    assert len(names) == 16, names
+    assert len(names) == 17, names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -161,3 +161,15 @@ def test_router_rejects_on_host(lib):
     assert f(None, None, 4, 256, 8, A16, A16, None) == binding.ERR_INVALID_ARG
     assert f(A16, P(0x10002), 4, 256, 8, A16, A16, None) == binding.ERR_INVALID_ARG  # misaligned bias
     assert f(None, None, 0, 256, 8, None, None, None) == binding.OK
+
+
+def test_quantize_rejects_on_host(lib):
+    P = ctypes.c_void_p
+    f = lib.wna16_moe_quantize
+    assert f(A16, 4, 4096, None, 3, 128, 1, A16, A16, None, None) == binding.ERR_UNSUPPORTED      # bits
+    assert f(A16, 4, 4096, None, 2, 48, 1, A16, A16, None, None) == binding.ERR_UNSUPPORTED       # group
+    assert f(A16, 4, 4096, None, 2, 16, 1, A16, A16, None, None) == binding.ERR_UNSUPPORTED       # 256 groups
+    assert f(A8, 4, 4096, None, 2, 128, 1, A16, A16, None, None) == binding.ERR_INVALID_ARG       # w alignment
+    assert f(A16, 4, 4096, None, 2, 128, 2, A16, A16, None, None) == binding.ERR_INVALID_ARG      # search flag
+    assert f(A16, 4, 4096, P(0x10004), 2, 128, 1, A16, A16, None, None) == binding.ERR_INVALID_ARG
+    assert f(None, 0, 4096, None, 2, 128, 1, None, None, None, None) == binding.OK

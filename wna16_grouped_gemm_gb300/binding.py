@@ -81,6 +81,8 @@ def load_library(path: str = LIB_PATH):
     lib.wna16_moe_forward_partial.restype = I
     lib.wna16_moe_forward_partial.argtypes = [P, P, P, P, P, P, P, I64, I64, I64, I64, I64, I64, I, I, I, I, F, P,
                                               P, SZ, P]
+    lib.wna16_moe_quantize.restype = I
+    lib.wna16_moe_quantize.argtypes = [P, I64, I64, P, I, I, I, P, P, P, P]
     lib.wna16_moe_route_topk.restype = I
     lib.wna16_moe_route_topk.argtypes = [P, P, I64, I64, I, P, P, P]
     lib.wna16_moe_combine.restype = I
@@ -251,6 +253,24 @@ def route_topk(logits, topk: int, bias=None, ids=None, weights=None, stream=None
     _check(load_library().wna16_moe_route_topk(_ptr(logits), _ptr(bias), T, E, topk, _ptr(ids), _ptr(weights),
                                                _stream(stream)))
     return ids, weights
+
+
+def quantize(w, bits: int, group_size: int = 128, importance=None, search: bool = True, metrics: bool = True,
+             stream=None):
+    """Symmetric RTN with an importance-weighted scale search: fp32 w
+    [rows, K] (+ importance [K]) -> (packed int32 [rows, K*bits/32], scales
+    fp16 [rows, K/group_size], metrics fp64 [rows, 4] or None)."""
+    _need(w, torch.float32, "w", 2)
+    rows, K = w.shape
+    if importance is not None:
+        _need(importance, torch.float32, "importance", 1)
+    packed = torch.empty(rows, K * bits // 32, dtype=torch.int32, device=w.device)
+    scales = torch.empty(rows, K // group_size, dtype=torch.float16, device=w.device)
+    met = torch.empty(rows, 4, dtype=torch.float64, device=w.device) if metrics else None
+    _check(load_library().wna16_moe_quantize(_ptr(w), rows, K, _ptr(importance), bits, group_size,
+                                             1 if search else 0, _ptr(packed), _ptr(scales), _ptr(met),
+                                             _stream(stream)))
+    return packed, scales, met
 
 
 STAGES = ("route", "gather", "w13", "w2", "combine")

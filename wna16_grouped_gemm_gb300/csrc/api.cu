@@ -608,6 +608,34 @@ int wna16_moe_route_topk(const float* logits, const float* bias, int64_t T, int6
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "router kernel launch");
 }
 
+int wna16_moe_quantize(const float* w, int64_t rows, int64_t K, const float* importance, int bits, int group_size,
+                       int search, int32_t* packed, uint16_t* scales, double* metrics, void* stream) {
+    g_err[0] = 0;
+    if (bits != 2 && bits != 4) return fail(WNA16_ERR_UNSUPPORTED, "bits=%d: only 2 and 4 are supported", bits);
+    if (rows < 0 || K <= 0) return fail(WNA16_ERR_INVALID_ARG, "rows=%lld must be >= 0 and K=%lld > 0",
+                                        (long long)rows, (long long)K);
+    if (group_size <= 0 || group_size % 32 || K % group_size)
+        return fail(WNA16_ERR_UNSUPPORTED, "group_size=%d must be a multiple of 32 dividing K=%lld", group_size,
+                    (long long)K);
+    if (K / group_size > 128)
+        return fail(WNA16_ERR_UNSUPPORTED, "K/group_size=%lld: at most 128 groups per row",
+                    (long long)(K / group_size));
+    if (K >= (int64_t(1) << 31) || rows * K >= (int64_t(1) << 62))
+        return fail(WNA16_ERR_UNSUPPORTED, "sizes too large");
+    if (search != 0 && search != 1) return fail(WNA16_ERR_INVALID_ARG, "search=%d must be 0 or 1", search);
+    if (rows == 0) return WNA16_OK;
+    if (int rc = check_ptr(w, 16, "w")) return rc;
+    if (importance)
+        if (int rc = check_ptr(importance, 16, "importance")) return rc;
+    if (int rc = check_ptr(packed, 4, "packed")) return rc;
+    if (int rc = check_ptr(scales, 2, "scales")) return rc;
+    if (metrics)
+        if (int rc = check_ptr(metrics, 8, "metrics")) return rc;
+    cudaError_t e = launch_quantize(w, rows, static_cast<int>(K), importance, bits, group_size, search, packed, scales,
+                                    metrics, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "quantize kernel launch");
+}
+
 int wna16_moe_launches_last_forward(void) { return g_launches; }
 
 int wna16_moe_profile(int slots) {

@@ -95,6 +95,10 @@ cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const in
 //   out[t, m] = bf16( sum_j w[t, j] * bf16(sum_s partial[s][m/256][inv[t, j]][m%256]) )
 cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
                                     int T, int topk, int K, void* out, bool f32_out, cudaStream_t stream);
+// Quantiser (quant.cu): packed [rows, K/p], scales fp16 [rows, K/g], metrics
+// fp64 [rows, 4] (or null) from fp32 w [rows, K] and importance [K] (or null).
+cudaError_t launch_quantize(const float* w, int64_t rows, int K, const float* importance, int bits, int g, int search,
+                            int32_t* packed, uint16_t* scales, double* metrics, cudaStream_t stream);
 cudaError_t launch_pack(const int8_t* codes, int64_t rows, int64_t K, int bits, int32_t* packed,
                         cudaStream_t stream);
 // One bounded mbarrier wait that nothing completes (device failure-detection check).
