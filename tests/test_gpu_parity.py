@@ -81,6 +81,34 @@ def test_route_bit_exact(moe, oracle, T, topk, E, zipf):
     assert np.array_equal(inv.cpu().numpy(), ri)
 
 
+def test_route_chunked_bad_ids_and_expert_range(moe, oracle):
+    """Large batches are routed by chunks in three kernels: an out-of-range id
+    anywhere sets the status word and its slot gets inv = -1, and the other
+    slots' lists are still bit-exact."""
+    T, topk, E = 3000, 8, 256
+    w = synth.Workload("r", T=T, K=256, N=128, E=E, topk=topk, bits=2, g13=128, g2=128, scale_lo=0.01,
+                       scale_hi=0.02)
+    ids, _ = synth.make_routing(w, seed=4)
+    bad = ids.copy()
+    bad[2999, 7] = E + 3
+    bad[5, 0] = -2
+    ws = moe.alloc_workspace(T, w.K, w.N, E, topk, w.bits)
+    counts, offsets, perm, inv = moe.route(torch.from_numpy(bad).cuda(), E, w.K, w.N, w.bits, workspace=ws)
+    assert moe.read_status(ws) == moe.ERR_BAD_ROUTING
+    inv = inv.cpu().numpy()
+    assert inv[2999 * topk + 7] == -1 and inv[5 * topk] == -1
+    good = np.ones(T * topk, bool)
+    good[[2999 * topk + 7, 5 * topk]] = False
+    flat = bad.ravel()
+    rc = np.bincount(flat[good], minlength=E)
+    assert np.array_equal(counts.cpu().numpy(), rc)
+    rp = np.nonzero(good)[0][np.argsort(flat[good], kind="stable")]
+    assert np.array_equal(perm.cpu().numpy()[:good.sum()], rp)
+    # a clean batch on the same workspace resets the status
+    moe.route(torch.from_numpy(ids).cuda(), E, w.K, w.N, w.bits, workspace=ws)
+    assert moe.read_status(ws) == moe.OK
+
+
 # ---------------------------------------------------------------- stages
 
 STAGE_CASES = [

@@ -82,9 +82,30 @@ int stage_k(int nt, int bits, int64_t kred) {
     return kp;
 }
 
-int choose_split(int64_t max_units, int64_t kred, int kp, int group) {
+// The tensor cores' fp32 accumulation in TMEM loses low-order bits on every
+// MMA K-step (the error grows with the number of steps added into one
+// accumulator and leans toward smaller magnitudes); measured against the
+// oracle on the 8192-token W4 prefill, 256 K-steps into one accumulator put
+// the output at relative L2 1.03e-3, 128 steps at 7.3e-4, 64 at 5.5e-4.  So
+// no accumulator takes more than kMaxChain K-steps of 16 before its sum is
+// added in fp32 on the CUDA cores: with one accumulator per row block (token
+// tiles above 32 rows) the K range is split until each split has at most
+// kMaxChain * 16 elements; smaller tiles alternate two accumulators per row
+// block (2 * kMaxChain steps per split), and the 2-bit group-accumulate mode
+// restarts its accumulator every scale group.
+constexpr int64_t kMaxChain = 128;
+
+int min_split_for_chain(int nt, int64_t kred) {
+    const int64_t per_acc = nt > 32 ? kMaxChain * 16 : 2 * kMaxChain * 16;
     int S = 1;
-    while (S < 8 && max_units * S < kTargetItems) {
+    while (S < 8 && kred / S > per_acc) S *= 2;
+    return S;
+}
+
+int choose_split(int64_t max_units, int64_t kred, int kp, int group, int nt) {
+    int S = 1;
+    const int need = min_split_for_chain(nt, kred);
+    while (S < 8 && (max_units * S < kTargetItems || S < need)) {
         const int64_t next = 2 * S;
         if ((kred / kp) % next || (kred / next) % group) break;
         S = static_cast<int>(next);
@@ -98,6 +119,7 @@ struct Layout {
     int64_t max_tiles = 0;
     int64_t units13 = 0, units2 = 0;      // largest possible unit counts of the two GEMMs
     size_t status = 0, n_tiles = 0, counts = 0, offsets = 0, perm = 0, inv = 0, tiles = 0, xp = 0, h = 0, y = 0;
+    size_t chunks = 0;                    // chunked routing scratch: [chunks][E] + [chunks] ints
     size_t partial = 0;
     size_t csum13 = 0, csum2 = 0;         // offset-code corrections (2-bit, 16-token tiles): [groups][R]
     size_t total = 0;
@@ -112,8 +134,8 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.units2 = L.max_tiles * (K / 256);
     // split-K partial sums for the largest split any group size could give (32
     // is the smallest supported group): splits x row tiles x R token rows x 256
-    const int64_t s13 = choose_split(L.units13, K, stage_k(L.nt, bits, K), 32);
-    const int64_t s2 = choose_split(L.units2, N, stage_k(L.nt, bits, N), 32);
+    const int64_t s13 = choose_split(L.units13, K, stage_k(L.nt, bits, K), 32, L.nt);
+    const int64_t s2 = choose_split(L.units2, N, stage_k(L.nt, bits, N), 32, L.nt);
     const int64_t p13 = s13 > 1 ? s13 * (N / 128) * L.R * 256 : 0;
     const int64_t p2 = s2 > 1 ? s2 * (K / 256) * L.R * 256 : 0;
     const int64_t partial_floats = p13 > p2 ? p13 : p2;
@@ -125,6 +147,7 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.perm = o;     o = align_up(o + sizeof(int) * L.R);
     L.inv = o;      o = align_up(o + sizeof(int) * L.R);
     L.tiles = o;    o = align_up(o + sizeof(int4) * L.max_tiles);
+    L.chunks = o;   o = align_up(o + sizeof(int) * static_cast<size_t>(route_chunks(static_cast<int>(L.R))) * (E + 1));
     L.xp = o;       o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
     L.h = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * N);
     L.y = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
@@ -286,7 +309,8 @@ int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStre
     cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), static_cast<int>(e_begin),
                                  static_cast<int>(E_total < 0 ? E : E_total), L.nt, at<int>(ws, L.counts),
                                  at<int>(ws, L.offsets), at<int>(ws, L.perm), at<int>(ws, L.inv),
-                                 at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status), s);
+                                 at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status),
+                                 at<int>(ws, L.chunks), s);
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "route kernel launch");
 }
 
@@ -313,7 +337,7 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     const int kp = stage_k(nt, bits, kred);
     const int pitch = kp * bits / 8;
     const int64_t max_units = w13 ? L.units13 : L.units2;
-    const int ksplit = choose_split(max_units, kred, kp, group);
+    const int ksplit = choose_split(max_units, kred, kp, group, nt);
     const int ngroups = static_cast<int>(kred / group);
     GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups / ksplit, dev.max_smem);
     if (sm.nstage < 2)

@@ -65,10 +65,14 @@ cudaError_t ensure_dynamic_smem(const void* fn, int bytes);
 
 // Routing / gather / combine / pack kernels (kernels.cu).
 // Routing lists of the local experts [e_begin, e_begin + E) among E_total
-// (e_begin = 0, E_total = E on a single device).
+// (e_begin = 0, E_total = E on a single device).  Batches of more than
+// kRouteChunkedMin slots are sorted by chunks in three kernels, with
+// route_chunks(R) * (E + 1) ints of chunk_scratch; smaller ones by one CTA.
+constexpr int kRouteChunkedMin = 8192;
+int route_chunks(int R);
 cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int* counts,
                          int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles, int* status,
-                         cudaStream_t stream);
+                         int* chunk_scratch, cudaStream_t stream);
 // Router: ids/weights [T, k] from fp32 logits [T, E] (+ bias [E] or null);
 // 1 <= k <= min(E, 32), E <= 1024.
 cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,

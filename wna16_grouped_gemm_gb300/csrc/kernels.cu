@@ -152,6 +152,118 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     }
 }
 
+// ---- routing lists for large batches: a stable counting sort in three
+// kernels over chunks of kChunk slots (the single-CTA route_kernel walks every
+// slot on one SM, which dominates at tens of thousands of slots).
+//   count: per chunk, the slots of each local expert  -> ccount[chunk][E]
+//   scan:  per expert, the chunks' starting positions (chunk order), the
+//          counts, offsets and the token-tile list        (one CTA)
+//   place: per chunk, each slot's position, stable in slot order
+constexpr int kChunk = 1024;
+constexpr int kChunkThreads = 256;
+constexpr int kChunkWarps = kChunkThreads / 32;
+
+__global__ void __launch_bounds__(kChunkThreads)
+    route_count_kernel(const int32_t* __restrict__ ids, int R, int E, int e_begin, int E_total,
+                       int* __restrict__ ccount, int* __restrict__ cbad) {
+    extern __shared__ int hist[];   // [E]
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+    __syncthreads();
+    const int f0 = blockIdx.x * kChunk;
+    const int f1 = min(R, f0 + kChunk);
+    bool bad = false;
+    for (int f = f0 + threadIdx.x; f < f1; f += blockDim.x) {
+        const int e = local_expert(ids[f], e_begin, E, E_total, bad);
+        if (e >= 0) atomicAdd(&hist[e], 1);
+    }
+    const int any_bad = __syncthreads_or(bad ? 1 : 0);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) ccount[static_cast<int64_t>(blockIdx.x) * E + e] = hist[e];
+    if (threadIdx.x == 0) cbad[blockIdx.x] = any_bad;
+}
+
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_scan_kernel(int nchunks, int E, int nt, int* __restrict__ ccount, const int* __restrict__ cbad,
+                      int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ tiles,
+                      int* __restrict__ n_tiles, int* __restrict__ status) {
+    __shared__ int scratch[64];
+    const int tid = threadIdx.x;
+    if (tid == 0) {
+        int bad = 0;
+        for (int c = 0; c < nchunks; ++c) bad |= cbad[c];
+        *status = bad ? kStatusBadRouting : kStatusOk;
+    }
+    // per expert: the chunks' exclusive starts within the expert, in chunk order
+    int c_tot = 0;
+    if (tid < E) {
+        for (int c = 0; c < nchunks; ++c) {
+            int* p = ccount + static_cast<int64_t>(c) * E + tid;
+            const int v = *p;
+            *p = c_tot;
+            c_tot += v;
+        }
+    }
+    const int ntl = tid < E ? (c_tot + nt - 1) / nt : 0;
+    int off, toff, total, ttotal;
+    block_exclusive_scan2(c_tot, ntl, off, toff, total, ttotal, scratch);
+    if (tid < E) {
+        counts[tid] = c_tot;
+        offsets[tid] = off;
+        for (int j = 0; j < ntl; ++j) tiles[toff + j] = make_int4(tid, off + j * nt, min(nt, c_tot - j * nt), 0);
+        for (int c = 0; c < nchunks; ++c) ccount[static_cast<int64_t>(c) * E + tid] += off;
+    }
+    if (tid == 0) {
+        offsets[E] = total;
+        *n_tiles = ttotal;
+    }
+}
+
+__global__ void __launch_bounds__(kChunkThreads)
+    route_place_kernel(const int32_t* __restrict__ ids, int R, int E, int e_begin, int E_total,
+                       const int* __restrict__ cstart, int* __restrict__ perm, int* __restrict__ inv) {
+    extern __shared__ int wcnt[];   // [kChunkWarps][E]
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int per_warp = kChunk / kChunkWarps;
+    const int f0 = blockIdx.x * kChunk + warp * per_warp;
+    const int f1 = min(R, f0 + per_warp);
+    int* my = wcnt + warp * E;
+    for (int e = lane; e < E; e += 32) my[e] = 0;
+    __syncwarp();
+    for (int base = f0; base < f1; base += 32) {
+        const int f = base + lane;
+        bool ignored = false;
+        const int e = f < f1 ? local_expert(ids[f], e_begin, E, E_total, ignored) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+    }
+    __syncthreads();
+    // per expert: the warps' starts (warp order) after the chunk's start
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int c = cstart[static_cast<int64_t>(blockIdx.x) * E + e];
+        for (int w = 0; w < kChunkWarps; ++w) {
+            const int v = wcnt[w * E + e];
+            wcnt[w * E + e] = c;
+            c += v;
+        }
+    }
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int base = f0; base < f1; base += 32) {
+        const int f = base + lane;
+        bool ignored = false;
+        const int e = f < f1 ? local_expert(ids[f], e_begin, E, E_total, ignored) : -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        const int pos = e >= 0 ? my[e] + __popc(peers & lt) : -1;
+        __syncwarp();
+        if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
+        __syncwarp();
+        if (f < f1) {
+            if (e >= 0) perm[pos] = f;
+            inv[f] = pos;
+        }
+    }
+}
+
 // Router: one warp per token.  Lane l holds the scores z = logit + bias of
 // experts l, l + 32, ... (PL per lane).  k rounds of a warp-wide argmax (the
 // larger score wins, equal scores go to the lower expert index) pick the
@@ -514,8 +626,25 @@ __global__ void pack_kernel(const int8_t* __restrict__ codes, int64_t n_words, i
 
 }  // namespace
 
+int route_chunks(int R) { return R > kRouteChunkedMin ? (R + kChunk - 1) / kChunk : 0; }
+
 cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int* counts, int* offsets,
-                         int* perm, int* inv, int4* tiles, int* n_tiles, int* status, cudaStream_t stream) {
+                         int* perm, int* inv, int4* tiles, int* n_tiles, int* status, int* chunk_scratch,
+                         cudaStream_t stream) {
+    const int nchunks = route_chunks(R);
+    if (nchunks > 0) {
+        int* ccount = chunk_scratch;                                  // [nchunks][E]
+        int* cbad = chunk_scratch + static_cast<int64_t>(nchunks) * E; // [nchunks]
+        const int hsmem = E * static_cast<int>(sizeof(int));
+        const int psmem = kChunkWarps * E * static_cast<int>(sizeof(int));
+        cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_place_kernel), psmem);
+        if (e != cudaSuccess) return e;
+        route_count_kernel<<<nchunks, kChunkThreads, hsmem, stream>>>(ids, R, E, e_begin, E_total, ccount, cbad);
+        route_scan_kernel<<<1, kRouteThreads, 0, stream>>>(nchunks, E, nt, ccount, cbad, counts, offsets, tiles,
+                                                          n_tiles, status);
+        route_place_kernel<<<nchunks, kChunkThreads, psmem, stream>>>(ids, R, E, e_begin, E_total, ccount, perm, inv);
+        return cudaGetLastError();
+    }
     const int smem = (kRouteWarps * E + 64) * static_cast<int>(sizeof(int));
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_kernel), smem);
     if (e != cudaSuccess) return e;
