@@ -350,11 +350,12 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
         // weights: [words of a row][rows][the unit's two 128-row blocks], the
         // second block N rows (w13: up) or 128 rows (w2) after the first
         const uint64_t row_bytes = static_cast<uint64_t>(kred / p) * 4;
-        const uint64_t block_rows = w13 ? static_cast<uint64_t>(N) : 128;
+        const uint64_t brows = 128;
+        const uint64_t block_rows = w13 ? static_cast<uint64_t>(N) : brows;
         const uint64_t dims[3] = {static_cast<uint64_t>(kred / p),
                                   static_cast<uint64_t>(E * rows_per_expert) - block_rows, 2};
         const uint64_t strides[2] = {row_bytes, block_rows * row_bytes};
-        const uint32_t box[3] = {static_cast<uint32_t>(pitch / 4), 128, 2};
+        const uint32_t box[3] = {static_cast<uint32_t>(pitch / 4), static_cast<uint32_t>(brows), 2};
         if (int rc = encode_3d(&P.tm_w, CU_TENSOR_MAP_DATA_TYPE_INT32, wpacked, dims, strides, box,
                                swizzle_for_pitch(pitch)))
             return rc;
