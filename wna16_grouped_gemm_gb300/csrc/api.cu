@@ -551,13 +551,32 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
         return rc;
 
     mark(0, s);
-    if (int rc = run_route(topk_ids, E, L, workspace, s, e_begin, E_total)) return rc;
-    mark(1, s);
-    cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
-                                  at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
-                                  static_cast<int>(K), il ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
-                                  p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
-    if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+    int launches = 0;
+    cudaError_t e = cudaSuccess;
+    if (L.R <= kSmallRouteMax) {
+        // small batch: routing lists and gather in one kernel (the gather stage is folded into route)
+        e = launch_route_gather_small(topk_ids, static_cast<int>(L.R), static_cast<int>(E), static_cast<int>(e_begin),
+                                      static_cast<int>(E_total), L.nt, topk, at<int>(workspace, L.counts),
+                                      at<int>(workspace, L.offsets), at<int>(workspace, L.perm),
+                                      at<int>(workspace, L.inv), at<int4>(workspace, L.tiles),
+                                      at<int>(workspace, L.n_tiles), at<int>(workspace, L.status),
+                                      static_cast<const __nv_bfloat16*>(x), static_cast<int>(K), il ? 1 : 0,
+                                      at<__nv_bfloat16>(workspace, L.xp),
+                                      p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
+        if (e != cudaSuccess) return cuda_fail(e, "route/gather kernel launch");
+        launches += 1;
+        mark(1, s);
+    } else {
+        if (int rc = run_route(topk_ids, E, L, workspace, s, e_begin, E_total)) return rc;
+        launches += route_chunks(static_cast<int>(L.R)) > 0 ? 3 : 1;
+        mark(1, s);
+        e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
+                          at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk, static_cast<int>(K),
+                          il ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
+                          p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
+        if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
+        launches += 1;
+    }
     mark(2, s);
     if (int rc = launch_plan(p13, s)) return rc;
     if (p13.gp.ksplit > 1) {   // split K: fixed-order sum of the splits + SwiGLU -> h
@@ -580,7 +599,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     mark(5, s);
     mark_done();
-    g_launches = 5 + (p13.gp.ksplit > 1 ? 1 : 0);
+    g_launches = launches + 3 + (p13.gp.ksplit > 1 ? 1 : 0);   // + w13 (+ finalize), w2, combine
     return WNA16_OK;
 }
 

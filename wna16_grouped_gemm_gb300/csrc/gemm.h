@@ -73,6 +73,13 @@ int route_chunks(int R);
 cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int* counts,
                          int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles, int* status,
                          int* chunk_scratch, cudaStream_t stream);
+// Routing lists and the gather of x rows in one kernel for small batches
+// (R <= kSmallRouteMax slots, E <= 1024): one CTA per slot.
+constexpr int kSmallRouteMax = 512;
+cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int topk,
+                                      int* counts, int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles,
+                                      int* status, const __nv_bfloat16* x, int K, int interleave, __nv_bfloat16* xp,
+                                      float* csum, cudaStream_t stream);
 // Router: ids/weights [T, k] from fp32 logits [T, E] (+ bias [E] or null);
 // 1 <= k <= min(E, 32), E <= 1024.
 cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,

@@ -16,7 +16,7 @@ constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 
 // Block-wide exclusive scan of two values with warp-level inclusive scans
-// (shuffles) and one pass over the 32 warp totals.
+// (shuffles) and one pass over the warp totals (blocks of up to 32 warps).
 __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int& ea, int& eb, int& total_a, int& total_b,
                                                       int* scratch /* 64 ints */) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -36,7 +36,8 @@ __device__ __forceinline__ void block_exclusive_scan2(int a, int b, int& ea, int
     }
     __syncthreads();
     if (warp == 0) {
-        int va = scratch[lane], vb = scratch[32 + lane];
+        const int nw = static_cast<int>(blockDim.x >> 5);
+        int va = lane < nw ? scratch[lane] : 0, vb = lane < nw ? scratch[32 + lane] : 0;
 #pragma unroll
         for (int d = 1; d < 32; d <<= 1) {
             const int ta = __shfl_up_sync(0xffffffffu, va, d);
@@ -379,14 +380,9 @@ __device__ __forceinline__ float offset_sum16(const uint4& lo, const uint4& hi) 
 // (optionally in the interleaved 16-k order); with csum (interleaved order
 // only) also csum[g * R + i] = sum over the 128-element group g of
 // offset_weight(k) x[k].
-__global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
-                              const int* __restrict__ offsets_end, int R, int topk, int vec_per_row, int interleave,
-                              uint4* __restrict__ xp, float* __restrict__ csum) {
-    pdl_wait();
-    pdl_trigger();
-    const int i = blockIdx.x;
-    if (i >= *offsets_end) return;
-    const int64_t t = perm[i] / topk;
+// Copies token row t of x into permuted row i of xp (one CTA; see gather_kernel).
+__device__ __forceinline__ void gather_row(const uint4* __restrict__ x, int64_t t, int i, int R, int vec_per_row,
+                                           int interleave, uint4* __restrict__ xp, float* __restrict__ csum) {
     const uint4* src = x + t * vec_per_row;
     uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
     if (!interleave) {
@@ -413,6 +409,98 @@ __global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict
             }
         }
     }
+}
+
+__global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
+                              const int* __restrict__ offsets_end, int R, int topk, int vec_per_row, int interleave,
+                              uint4* __restrict__ xp, float* __restrict__ csum) {
+    pdl_wait();
+    pdl_trigger();
+    const int i = blockIdx.x;
+    if (i >= *offsets_end) return;
+    gather_row(x, perm[i] / topk, i, R, vec_per_row, interleave, xp, csum);
+}
+
+// Routing lists and the gather in one kernel, for small batches (decode):
+// one CTA per slot f.  Every CTA reads all R ids; slot f's position in the
+// stable (expert, slot) order is the number of valid slots that sort before
+// it, so no scan across CTAs is needed.  CTA f records perm / inv for its slot
+// and copies its token's row of x to that position; CTA 0 also writes the
+// per-expert counts and offsets, the token-tile list and the status word.
+constexpr int kSmallRouteThreads = 256;
+
+__global__ void __launch_bounds__(kSmallRouteThreads)
+    route_gather_small_kernel(const int32_t* __restrict__ ids, int R, int E, int e_begin, int E_total, int nt,
+                              int topk, int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm,
+                              int* __restrict__ inv, int4* __restrict__ tiles, int* __restrict__ n_tiles,
+                              int* __restrict__ status, const uint4* __restrict__ x, int vec_per_row, int interleave,
+                              uint4* __restrict__ xp, float* __restrict__ csum) {
+    extern __shared__ int sm[];
+    int* le = sm;                      // [R] local expert of each slot (-1: skipped or bad)
+    int* cnt = sm + R;                 // [E] (CTA 0)
+    __shared__ int red[kSmallRouteThreads / 32];
+    __shared__ int scratch[64];
+    pdl_trigger();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int f = blockIdx.x;
+    bool bad = false;
+    for (int q = tid; q < R; q += blockDim.x) le[q] = local_expert(ids[q], e_begin, E, E_total, bad);
+    const int any_bad = __syncthreads_or(bad ? 1 : 0);
+    const int e = le[f];
+    // rank of slot f among the valid slots in (expert, slot) order
+    int c = 0;
+    if (e >= 0)
+        for (int q = tid; q < R; q += blockDim.x) {
+            const int eq = le[q];
+            c += (eq >= 0 && (eq < e || (eq == e && q < f))) ? 1 : 0;
+        }
+#pragma unroll
+    for (int d = 16; d > 0; d >>= 1) c += __shfl_xor_sync(0xffffffffu, c, d);
+    if (lane == 0) red[warp] = c;
+    __syncthreads();
+    int rank = 0;
+    for (int w = 0; w < kSmallRouteThreads / 32; ++w) rank += red[w];
+    if (tid == 0) {
+        inv[f] = e >= 0 ? rank : -1;
+        if (e >= 0) perm[rank] = f;
+    }
+    if (f == 0) {
+        // counts, offsets, tiles, status
+        for (int q = tid; q < E; q += blockDim.x) cnt[q] = 0;
+        __syncthreads();
+        for (int q = tid; q < R; q += blockDim.x)
+            if (le[q] >= 0) atomicAdd(&cnt[le[q]], 1);
+        __syncthreads();
+        // E <= 1024 experts over 256 threads: each thread sums a run of 4 experts
+        int run[4], rtot = 0, rtiles = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = tid * 4 + j;
+            run[j] = q < E ? cnt[q] : 0;
+            rtot += run[j];
+            rtiles += (run[j] + nt - 1) / nt;
+        }
+        int off, toff, total, ttotal;
+        block_exclusive_scan2(rtot, rtiles, off, toff, total, ttotal, scratch);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int q = tid * 4 + j;
+            if (q < E) {
+                counts[q] = run[j];
+                offsets[q] = off;
+                const int ntl = (run[j] + nt - 1) / nt;
+                for (int k = 0; k < ntl; ++k) tiles[toff + k] = make_int4(q, off + k * nt, min(nt, run[j] - k * nt), 0);
+                off += run[j];
+                toff += ntl;
+            }
+        }
+        if (tid == 0) {
+            offsets[E] = total;
+            *n_tiles = ttotal;
+            *status = any_bad ? kStatusBadRouting : kStatusOk;
+        }
+    }
+    if (e >= 0 && xp) gather_row(x, f / topk, rank, R, vec_per_row, interleave, xp, csum);
 }
 
 __global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t blocks, int inverse,
@@ -667,6 +755,20 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
     if (pl <= 32)
         return launch_pdl(route_topk_kernel<32>, grid, block, 0, stream, logits, bias, T, E, k, ids, weights);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int topk,
+                                      int* counts, int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles,
+                                      int* status, const __nv_bfloat16* x, int K, int interleave, __nv_bfloat16* xp,
+                                      float* csum, cudaStream_t stream) {
+    if (R == 0) return cudaSuccess;
+    const int smem = (R + E) * static_cast<int>(sizeof(int));
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_gather_small_kernel), smem);
+    if (e != cudaSuccess) return e;
+    route_gather_small_kernel<<<R, kSmallRouteThreads, smem, stream>>>(
+        ids, R, E, e_begin, E_total, nt, topk, counts, offsets, perm, inv, tiles, n_tiles, status,
+        reinterpret_cast<const uint4*>(x), K / 8, interleave, reinterpret_cast<uint4*>(xp), interleave ? csum : nullptr);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
