@@ -52,6 +52,11 @@
  *   - Thread safety: calls are re-entrant; concurrent calls must not share a
  *     workspace.  All kernels are compiled ahead of time for sm_103a; nothing
  *     is compiled or loaded at run time.
+ *   - Bounds-checked build: the same sources compiled with -DWNA16_DEBUG
+ *     (libwna16_moe_debug.so) check every index the kernels compute from
+ *     routing and tile data (expert rows, permuted rows, split-K slots,
+ *     correction rows) and, instead of an out-of-bounds access, skip it and
+ *     store WNA16_ERR_INDEX in the status word.
  */
 #ifndef WNA16_MOE_H
 #define WNA16_MOE_H
@@ -77,7 +82,9 @@ typedef enum {
     WNA16_ERR_CUDA = -4,              /* a CUDA runtime call or launch failed            */
     /* device status word values (wna16_moe_read_status): */
     WNA16_ERR_BAD_ROUTING = -5,       /* an expert id was outside [0, E); its slot adds 0 */
-    WNA16_ERR_DEVICE_TIMEOUT = -6     /* a pipeline wait gave up; the output is invalid  */
+    WNA16_ERR_DEVICE_TIMEOUT = -6,    /* a pipeline wait gave up; the output is invalid  */
+    WNA16_ERR_INDEX = -7              /* bounds-checked build only: a computed index fell
+                                         outside its buffer; that access was skipped      */
 } wna16_status;
 
 /* Pack signed codes into INT32 words (page "hampsonw/DeepSeek-V4-Flash-0731-

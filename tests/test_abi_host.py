@@ -173,3 +173,11 @@ def test_quantize_rejects_on_host(lib):
     assert f(A16, 4, 4096, None, 2, 128, 2, A16, A16, None, None) == binding.ERR_INVALID_ARG      # search flag
     assert f(A16, 4, 4096, P(0x10004), 2, 128, 1, A16, A16, None, None) == binding.ERR_INVALID_ARG
     assert f(None, 0, 4096, None, 2, 128, 1, None, None, None, None) == binding.OK
+
+
+def test_debug_library_exports_the_same_symbols():
+    """The bounds-checked build is the same library with index checks on."""
+    build.build(debug=True)
+    dbg = binding.load_debug_library()
+    for n in binding.exported_names_in_header():
+        assert hasattr(dbg, n), n

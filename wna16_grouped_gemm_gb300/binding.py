@@ -16,6 +16,7 @@ import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libwna16_moe.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "libwna16_moe_debug.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "wna16_moe.h")
 
 OK = 0
@@ -25,8 +26,10 @@ ERR_WORKSPACE_TOO_SMALL = -3
 ERR_CUDA = -4
 ERR_BAD_ROUTING = -5
 ERR_DEVICE_TIMEOUT = -6
+ERR_INDEX = -7
 
 _lib = None
+_debug_lib = None
 
 
 class Wna16Error(RuntimeError):
@@ -46,6 +49,22 @@ def load_library(path: str = LIB_PATH):
     global _lib
     if _lib is not None:
         return _lib
+    _lib = _open(path)
+    return _lib
+
+
+def load_debug_library():
+    """The bounds-checked build of the same library (built with
+    build.build(debug=True)): same entry points, and an index that falls
+    outside its buffer sets the status word to ERR_INDEX instead of touching
+    memory out of bounds."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _open(DEBUG_LIB_PATH)
+    return _debug_lib
+
+
+def _open(path: str):
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with wna16_grouped_gemm_gb300.build.build() "
                            "(there is no non-CUDA implementation)")
@@ -87,7 +106,6 @@ def load_library(path: str = LIB_PATH):
     lib.wna16_moe_route_topk.argtypes = [P, P, I64, I64, I, P, P, P]
     lib.wna16_moe_combine.restype = I
     lib.wna16_moe_combine.argtypes = [P, P, I64, I64, I, I64, I64, I, P, P, SZ, P]
-    _lib = lib
     return lib
 
 

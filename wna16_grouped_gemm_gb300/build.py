@@ -18,6 +18,10 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libwna16_moe.so")
+# the bounds-checked build (-DWNA16_DEBUG): index checks that record
+# WNA16_ERR_INDEX in the status word instead of accessing out of bounds
+DEBUG_BUILD_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(HERE, "libwna16_moe_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
@@ -39,15 +43,15 @@ def _deps():
         glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
+def _compile(src: str, extra, build_dir: str = BUILD_DIR) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [_nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -57,22 +61,31 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Build the library if needed and return its path."""
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    """Build the library (or, with debug, the bounds-checked library) if
+    needed and return its path."""
+    lib = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if verbose_ptxas else []) + (["-DWNA16_DEBUG"] if debug else [])
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), _sources()))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, extra, build_dir), _sources()))
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [_nvcc(), *ARCH, "-shared", "-Xcompiler", "-fPIC", *objs, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False) -> None:
+    """The release and the bounds-checked library."""
+    build(force)
+    build(force, debug=True)
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -416,6 +416,7 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.ksplit = ksplit;
     gp.partial = ksplit > 1 ? at<float>(ws, L.partial) : nullptr;
     gp.partial_rows = static_cast<int>(L.R);
+    gp.n_weight_rows = E * rows_per_expert;
     gp.h_interleaved = h_interleaved ? 1 : 0;
     // widest async copy that divides the scale row stride, one split's row
     // segment and the base alignment
@@ -573,7 +574,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
         e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                           at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk, static_cast<int>(K),
                           il ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
-                          p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
+                          p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status), s);
         if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
         launches += 1;
     }
@@ -592,10 +593,11 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
     if (p2.gp.ksplit > 1)      // split K: the combine adds the splits itself
         e = launch_combine_partials(at<float>(workspace, L.partial), p2.gp.ksplit, static_cast<int>(L.R), topk_weights,
                                     at<int>(workspace, L.inv), static_cast<int>(T), topk, static_cast<int>(K), out,
-                                    f32_out, s);
+                                    f32_out, at<int>(workspace, L.status), s);
     else
         e = launch_combine(at<__nv_bfloat16>(workspace, L.y), topk_weights, at<int>(workspace, L.inv),
-                           static_cast<int>(T), topk, static_cast<int>(K), out, f32_out, s);
+                           static_cast<int>(T), topk, static_cast<int>(K), out, f32_out, static_cast<int>(L.R),
+                           at<int>(workspace, L.status), s);
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     mark(5, s);
     mark_done();
@@ -777,7 +779,8 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
     cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
                                   static_cast<int>(K), bits == 2 ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
-                                  p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
+                                  p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status),
+                                  s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     if (int rc = launch_plan(p13, s)) return rc;
     if (p13.gp.ksplit > 1) {
@@ -835,8 +838,8 @@ int wna16_moe_combine(const void* y, const float* topk_weights, int64_t T, int64
     const Layout L = make_layout(T, K, N, E, topk, bits);
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaError_t e = launch_combine(static_cast<const __nv_bfloat16*>(y), topk_weights, at<int>(workspace, L.inv),
-                                   static_cast<int>(T), topk, static_cast<int>(K), out, false,
-                                   static_cast<cudaStream_t>(stream));
+                                   static_cast<int>(T), topk, static_cast<int>(K), out, false, static_cast<int>(L.R),
+                                   at<int>(workspace, L.status), static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "combine kernel launch");
 }
 

@@ -402,6 +402,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     const int r = i / cpr;
                     const int c = i - r * cpr;
                     const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
+                    if (!in_bounds(grow >= 0 && grow < p.n_weight_rows, status)) continue;
                     const uint8_t* src =
                         reinterpret_cast<const uint8_t*>(p.scales + static_cast<int64_t>(grow) * ng + g0) + c * cb;
                     uint8_t* dd = dst + r * rb + c * cb;
@@ -417,6 +418,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 uint16_t* d16 = reinterpret_cast<uint16_t*>(dst);
                 for (int r = lane; r < 2 * kRowsPerTile; r += 32) {
                     const int grow = r < kRowsPerTile ? r0 + r : r1 + (r - kRowsPerTile);
+                    if (!in_bounds(grow >= 0 && grow < p.n_weight_rows, status)) continue;
                     const uint16_t* src = p.scales + static_cast<int64_t>(grow) * ng + g0;
                     for (int g = 0; g < ng_item; ++g) d16[r * ng_item + g] = __ldg(src + g);
                 }
@@ -558,7 +560,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     load(j0, s0, s1);
 #pragma unroll
                     for (int i = 0; i < kEW; ++i) {
-                        if (j0 + i < rows) {
+                        if (j0 + i < rows && in_bounds(row0 + j0 + i < R_rows, p.status)) {
                             mine[(j0 + i) * (2 * kRowsPerTile)] = s0[i];
                             mine[(j0 + i) * (2 * kRowsPerTile) + kRowsPerTile] = s1[i];
                         }
@@ -575,7 +577,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     load(j0, g, uu);
 #pragma unroll
                     for (int i = 0; i < kEW; ++i)
-                        if (j0 + i < rows)
+                        if (j0 + i < rows && in_bounds(row0 + j0 + i < p.partial_rows && n < p.out_ld, p.status))
                             p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + n] =
                                 __float2bfloat16_rn(swiglu(g[i], uu[i], L));
                 }
@@ -586,7 +588,8 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     load(j0, y0, y1);
 #pragma unroll
                     for (int i = 0; i < kEW; ++i) {
-                        if (j0 + i < rows) {
+                        if (j0 + i < rows &&
+                            in_bounds(row0 + j0 + i < p.partial_rows && m + kRowsPerTile < p.out_ld, p.status)) {
                             __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + j0 + i) * p.out_ld + m;
                             o[0] = __float2bfloat16_rn(y0[i]);
                             o[kRowsPerTile] = __float2bfloat16_rn(y1[i]);
@@ -604,7 +607,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                                               (2 * kRowsPerTile) + row;
 #pragma unroll
                 for (int i = 0; i < N; ++i) {
-                    if (i < rows) {
+                    if (i < rows && in_bounds(row0 + i < R_rows, p.status)) {
                         mine[i * (2 * kRowsPerTile)] = y0[i];
                         mine[i * (2 * kRowsPerTile) + kRowsPerTile] = y1[i];
                     }
@@ -616,13 +619,13 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 const int n = p.h_interleaved ? interleave16(n0) : n0;
 #pragma unroll
                 for (int i = 0; i < N; ++i)
-                    if (i < rows)
+                    if (i < rows && in_bounds(row0 + i < p.partial_rows && n < p.out_ld, p.status))
                         p.out[static_cast<int64_t>(row0 + i) * p.out_ld + n] = __float2bfloat16_rn(swiglu(y0[i], y1[i], L));
             } else {
                 const int m = mt * 2 * kRowsPerTile + row;
 #pragma unroll
                 for (int i = 0; i < N; ++i) {
-                    if (i < rows) {
+                    if (i < rows && in_bounds(row0 + i < p.partial_rows && m + kRowsPerTile < p.out_ld, p.status)) {
                         __nv_bfloat16* o = p.out + static_cast<int64_t>(row0 + i) * p.out_ld + m;
                         o[0] = __float2bfloat16_rn(y0[i]);
                         o[kRowsPerTile] = __float2bfloat16_rn(y1[i]);
@@ -665,7 +668,10 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                             float cs[8];
 #pragma unroll
                             for (int i = 0; i < 8; ++i)
-                                cs[i] = goff && i < tile.z ? __ldg(crow + static_cast<int64_t>(g) * R_rows + i) : 0.0f;
+                                cs[i] = goff && i < tile.z &&
+                                                in_bounds(tile.y + i < R_rows && split * ng_item + g < p.ngroups, status)
+                                            ? __ldg(crow + static_cast<int64_t>(g) * R_rows + i)
+                                            : 0.0f;
                             if (!mbar_wait(&gfull[gs.idx], gs.phase, abort_flag, status)) {
                                 ok = false;
                                 break;
@@ -711,7 +717,9 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                                 float cs[8];
 #pragma unroll
                                 for (int i = 0; i < 8; ++i)
-                                    cs[i] = goff && q + i < tile.z
+                                    cs[i] = goff && q + i < tile.z &&
+                                                    in_bounds(tile.y + q + i < R_rows &&
+                                                                  split * ng_item + g < p.ngroups, status)
                                                 ? __ldg(crow + static_cast<int64_t>(g) * R_rows + q + i)
                                                 : 0.0f;
                                 uint32_t d0[8], d1[8];

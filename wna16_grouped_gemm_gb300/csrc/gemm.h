@@ -35,6 +35,7 @@ struct GemmParams {
     int ksplit;                 // K splits per unit (1: no split)
     float* partial;             // split-K partial sums [ksplit][mt_count][partial_rows][256] fp32
     int partial_rows;           // rows of the permuted token order (R)
+    int64_t n_weight_rows;      // E * rows_per_expert (bound of the scale rows, bounds-checked build)
     int h_interleaved;          // w13: store h columns in the interleaved 16-k order (2-bit w2 input)
     int scale_copy_bytes;       // 16, 8 or 4: cp.async size for the scale rows; 0: plain loads
     const float* csum;          // GA mode with offset codes: per scale group and permuted token row,
@@ -87,14 +88,14 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
 // With csum (2-bit interleaved order only, group 128): also the offset-code
 // corrections of the gathered rows, csum[g * R + i] = sum over group g of w(k) x.
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
-                          int K, int interleave, __nv_bfloat16* xp, float* csum, cudaStream_t stream);
+                          int K, int interleave, __nv_bfloat16* xp, float* csum, int* status, cudaStream_t stream);
 // dst[i, :] = src[i, :] with every 16-element block in the interleaved K order
 // (0, 8, 1, 9, ..., 7, 15) (or back, with inverse = 1).
 cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
                                    __nv_bfloat16* dst, cudaStream_t stream);
 // out bf16 [T, K], or with f32_out the unrounded fp32 sums (partial output)
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
-                           void* out, bool f32_out, cudaStream_t stream);
+                           void* out, bool f32_out, int R, int* status, cudaStream_t stream);
 // Split-K epilogues (partial sums [ksplit][mt][R][256] fp32, rows < offsets_end):
 //   h[r, n] = bf16(swiglu(sum_s gate, sum_s up)) (column n at its interleaved position if `interleave`),
 //   and with csum the offset-code corrections of h for w2 (group 128), csum[g * R + r]
@@ -105,7 +106,7 @@ cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const in
                                __nv_bfloat16* y, cudaStream_t stream);
 //   out[t, m] = bf16( sum_j w[t, j] * bf16(sum_s partial[s][m/256][inv[t, j]][m%256]) )
 cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
-                                    int T, int topk, int K, void* out, bool f32_out, cudaStream_t stream);
+                                    int T, int topk, int K, void* out, bool f32_out, int* status, cudaStream_t stream);
 // Quantiser (quant.cu): packed [rows, K/p], scales fp16 [rows, K/g], metrics
 // fp64 [rows, 4] (or null) from fp32 w [rows, K] and importance [K] (or null).
 cudaError_t launch_quantize(const float* w, int64_t rows, int K, const float* importance, int bits, int g, int search,

@@ -147,7 +147,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
         if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
         __syncwarp();
         if (f < f1) {
-            if (e >= 0) perm[pos] = f;
+            if (e >= 0 && in_bounds(pos >= 0 && pos < R, status)) perm[pos] = f;
             inv[f] = pos;
         }
     }
@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 
 __global__ void __launch_bounds__(kChunkThreads)
     route_place_kernel(const int32_t* __restrict__ ids, int R, int E, int e_begin, int E_total,
-                       const int* __restrict__ cstart, int* __restrict__ perm, int* __restrict__ inv) {
+                       const int* __restrict__ cstart, int* __restrict__ perm, int* __restrict__ inv,
+                       int* __restrict__ status) {
     extern __shared__ int wcnt[];   // [kChunkWarps][E]
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int per_warp = kChunk / kChunkWarps;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kChunkThreads)
         if (e >= 0 && lane == __ffs(peers) - 1) my[e] += __popc(peers);
         __syncwarp();
         if (f < f1) {
-            if (e >= 0) perm[pos] = f;
+            if (e >= 0 && in_bounds(pos >= 0 && pos < R, status)) perm[pos] = f;
             inv[f] = pos;
         }
     }
@@ -413,12 +414,14 @@ __device__ __forceinline__ void gather_row(const uint4* __restrict__ x, int64_t 
 
 __global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
                               const int* __restrict__ offsets_end, int R, int topk, int vec_per_row, int interleave,
-                              uint4* __restrict__ xp, float* __restrict__ csum) {
+                              uint4* __restrict__ xp, float* __restrict__ csum, int* __restrict__ status) {
     pdl_wait();
     pdl_trigger();
     const int i = blockIdx.x;
     if (i >= *offsets_end) return;
-    gather_row(x, perm[i] / topk, i, R, vec_per_row, interleave, xp, csum);
+    const int f = perm[i];
+    if (!in_bounds(f >= 0 && f < R, status)) return;
+    gather_row(x, f / topk, i, R, vec_per_row, interleave, xp, csum);
 }
 
 // Routing lists and the gather in one kernel, for small batches (decode):
@@ -460,9 +463,10 @@ __global__ void __launch_bounds__(kSmallRouteThreads)
     __syncthreads();
     int rank = 0;
     for (int w = 0; w < kSmallRouteThreads / 32; ++w) rank += red[w];
+    const bool rank_ok = e < 0 || in_bounds(rank < R, status);
     if (tid == 0) {
-        inv[f] = e >= 0 ? rank : -1;
-        if (e >= 0) perm[rank] = f;
+        inv[f] = e >= 0 && rank_ok ? rank : -1;
+        if (e >= 0 && rank_ok) perm[rank] = f;
     }
     if (f == 0) {
         // counts, offsets, tiles, status
@@ -500,7 +504,7 @@ __global__ void __launch_bounds__(kSmallRouteThreads)
             *status = any_bad ? kStatusBadRouting : kStatusOk;
         }
     }
-    if (e >= 0 && xp) gather_row(x, f / topk, rank, R, vec_per_row, interleave, xp, csum);
+    if (e >= 0 && rank_ok && xp) gather_row(x, f / topk, rank, R, vec_per_row, interleave, xp, csum);
 }
 
 __global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t blocks, int inverse,
@@ -522,7 +526,7 @@ __global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t bl
 // partial output of an expert range).
 template <bool F32OUT>
 __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restrict__ w, const int* __restrict__ inv,
-                               int topk, int vec_per_row, void* __restrict__ out) {
+                               int topk, int vec_per_row, void* __restrict__ out, int R, int* __restrict__ status) {
     pdl_wait();
     const int t = blockIdx.x;
     const int v = blockIdx.y * blockDim.x + threadIdx.x;
@@ -530,7 +534,7 @@ __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restr
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     for (int j = 0; j < topk; ++j) {
         const int r = inv[t * topk + j];
-        if (r < 0) continue;
+        if (r < 0 || !in_bounds(r < R, status)) continue;
         const float wj = w[t * topk + j];
         const uint4 q = __ldg(y + static_cast<int64_t>(r) * vec_per_row + v);
         const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
@@ -636,7 +640,8 @@ __global__ void finalize_w2_kernel(const float* __restrict__ partial, int ksplit
 // together.
 template <int KS, bool F32OUT>
 __global__ void combine_partials_kernel(const float* __restrict__ partial, int R, const float* __restrict__ w,
-                                        const int* __restrict__ inv, int topk, int K, void* __restrict__ out) {
+                                        const int* __restrict__ inv, int topk, int K, void* __restrict__ out,
+                                        int* __restrict__ status) {
     pdl_wait();
     const int t = blockIdx.x;
     const int lane = threadIdx.x & 31;
@@ -664,6 +669,7 @@ __global__ void combine_partials_kernel(const float* __restrict__ partial, int R
                 r[b] = __shfl_sync(0xffffffffu, rl, (j + b) & 31);
                 wj[b] = __shfl_sync(0xffffffffu, wl, (j + b) & 31);
                 if (j + b >= jn || !active) r[b] = -1;
+                if (r[b] >= 0 && !in_bounds(r[b] < R, status)) r[b] = -1;
             }
             float4 q[JB][KS];
 #pragma unroll
@@ -730,7 +736,8 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_to
         route_count_kernel<<<nchunks, kChunkThreads, hsmem, stream>>>(ids, R, E, e_begin, E_total, ccount, cbad);
         route_scan_kernel<<<1, kRouteThreads, 0, stream>>>(nchunks, E, nt, ccount, cbad, counts, offsets, tiles,
                                                           n_tiles, status);
-        route_place_kernel<<<nchunks, kChunkThreads, psmem, stream>>>(ids, R, E, e_begin, E_total, ccount, perm, inv);
+        route_place_kernel<<<nchunks, kChunkThreads, psmem, stream>>>(ids, R, E, e_begin, E_total, ccount, perm, inv,
+                                                                      status);
         return cudaGetLastError();
     }
     const int smem = (kRouteWarps * E + 64) * static_cast<int>(sizeof(int));
@@ -772,12 +779,13 @@ cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_be
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
-                          int interleave, __nv_bfloat16* xp, float* csum, cudaStream_t stream) {
+                          int interleave, __nv_bfloat16* xp, float* csum, int* status, cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
     const int vpr = K / 8;
     const int threads = vpr >= 256 ? 256 : 32;
     return launch_pdl(gather_kernel, dim3(R), dim3(threads), 0, stream, reinterpret_cast<const uint4*>(x), perm,
-                      offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp), interleave ? csum : nullptr);
+                      offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp), interleave ? csum : nullptr,
+                      status);
 }
 
 cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
@@ -791,16 +799,16 @@ cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64
 }
 
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
-                           void* out, bool f32_out, cudaStream_t stream) {
+                           void* out, bool f32_out, int R, int* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
     const int vpr = K / 8;
     const int threads = 128;
     const dim3 grid(T, (vpr + threads - 1) / threads);
     if (f32_out)
         return launch_pdl(combine_kernel<true>, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y),
-                          weights, inv, topk, vpr, out);
+                          weights, inv, topk, vpr, out, R, status);
     return launch_pdl(combine_kernel<false>, grid, dim3(threads), 0, stream, reinterpret_cast<const uint4*>(y), weights,
-                      inv, topk, vpr, out);
+                      inv, topk, vpr, out, R, status);
 }
 
 cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
@@ -827,25 +835,26 @@ cudaError_t launch_finalize_w2(const float* partial, int ksplit, int R, const in
 
 template <bool F32OUT>
 static cudaError_t launch_combine_partials_t(const float* partial, int ksplit, int R, const float* weights,
-                                             const int* inv, int T, int topk, int K, void* out, cudaStream_t stream) {
+                                             const int* inv, int T, int topk, int K, void* out, int* status,
+                                             cudaStream_t stream) {
     const int threads = 128;
     const dim3 grid(T, (K / 4 + threads - 1) / threads);
     switch (ksplit) {
         case 2: return launch_pdl(combine_partials_kernel<2, F32OUT>, grid, dim3(threads), 0, stream, partial, R,
-                                  weights, inv, topk, K, out);
+                                  weights, inv, topk, K, out, status);
         case 4: return launch_pdl(combine_partials_kernel<4, F32OUT>, grid, dim3(threads), 0, stream, partial, R,
-                                  weights, inv, topk, K, out);
+                                  weights, inv, topk, K, out, status);
         case 8: return launch_pdl(combine_partials_kernel<8, F32OUT>, grid, dim3(threads), 0, stream, partial, R,
-                                  weights, inv, topk, K, out);
+                                  weights, inv, topk, K, out, status);
         default: return cudaErrorInvalidValue;
     }
 }
 
 cudaError_t launch_combine_partials(const float* partial, int ksplit, int R, const float* weights, const int* inv,
-                                    int T, int topk, int K, void* out, bool f32_out, cudaStream_t stream) {
+                                    int T, int topk, int K, void* out, bool f32_out, int* status, cudaStream_t stream) {
     if (T == 0) return cudaSuccess;
-    return f32_out ? launch_combine_partials_t<true>(partial, ksplit, R, weights, inv, T, topk, K, out, stream)
-                   : launch_combine_partials_t<false>(partial, ksplit, R, weights, inv, T, topk, K, out, stream);
+    return f32_out ? launch_combine_partials_t<true>(partial, ksplit, R, weights, inv, T, topk, K, out, status, stream)
+                   : launch_combine_partials_t<false>(partial, ksplit, R, weights, inv, T, topk, K, out, status, stream);
 }
 
 // One bounded pipeline wait on a barrier that nothing completes: the wait

@@ -32,6 +32,21 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 constexpr int kStatusOk = 0;
 constexpr int kStatusBadRouting = -5;
 constexpr int kStatusTimeout = -6;
+constexpr int kStatusIndex = -7;
+
+// Index checks of the bounds-checked build (compiled with -DWNA16_DEBUG): an
+// index computed from routing or tile data that falls outside its buffer
+// records kStatusIndex in the status word and the access is skipped, instead
+// of touching memory out of bounds.  In the release build the check is the
+// constant true and compiles away.
+#ifdef WNA16_DEBUG
+__device__ __forceinline__ bool in_bounds(bool ok, int* status) {
+    if (!ok) atomicExch(status, kStatusIndex);
+    return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, int*) { return true; }
+#endif
 
 // A pipeline wait that has not completed after this long gives up: the CTA
 // records kStatusTimeout and unwinds.  Real waits last microseconds.
