@@ -77,11 +77,18 @@ WORKLOADS["prefill_w2_zipf_tp4"] = dataclasses.replace(WORKLOADS["prefill_w2_zip
 
 
 def get(name: str) -> Workload:
+    """A named workload; "<name>_T<tokens>" changes the token count and
+    "<name>_E<experts>_T<tokens>" also the expert count (a smaller problem of
+    the same shape, e.g. for a profiler capture)."""
     if name in WORKLOADS:
         return WORKLOADS[name]
     base, _, t = name.rpartition("_T")
     if base in WORKLOADS and t.isdigit():
         return WORKLOADS[base].with_tokens(int(t))
+    b2, _, e = base.rpartition("_E")
+    if b2 in WORKLOADS and e.isdigit() and t.isdigit():
+        w = dataclasses.replace(WORKLOADS[b2], E=int(e), name=name)
+        return dataclasses.replace(w, T=int(t))
     raise KeyError(name)
 
 

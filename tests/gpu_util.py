@@ -57,6 +57,7 @@ def compare_bf16(got_bits, ref_bits, what: str = "") -> dict:
                  max_abs_excess=float((d - allowed).max()) if d.size else 0.0,
                  # elements inside the bar only through the one-ulp allowance for |ref| >= 4
                  widened=int((d > MAX_ABS).sum()),
+                 beyond=int((d > allowed).sum()),
                  exact=float((ulp == 0).mean()) if ulp.size else 1.0,
                  le1ulp=float((ulp <= 1).mean()) if ulp.size else 1.0,
                  nonfinite=int((~np.isfinite(g)).sum()))
