@@ -474,3 +474,38 @@ def test_scale_doubling_is_exact_on_gpu(moe):
     d2 = dict(d, w2_scales=(d["w2_scales"].float() * 2).half())
     b, _ = _gpu_fwd(moe, w, d2)
     assert torch.equal(b.float(), 2 * a.float())
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("E", [1, 4])
+def test_dequant_exact_every_fp16_scale(moe, oracle, bits, E):
+    """The w2 stage on one-hot h rows returns single dequantised weights:
+    y[r, m] = bf16(code[m, n_r] * s[m, n_r / 128]) bit for bit, with the w2
+    scales running over every non-negative finite fp16 value and the codes
+    over every value (E = 1: 16-row tiles of plain dequantisation; E = 4:
+    4-token tiles, which take the group-accumulate mode for 2-bit).  A one-hot
+    column at the wrong place of the interleaved K order would also show."""
+    T, K, N, g = 16, 4096, 2048, 128
+    rng = np.random.default_rng(11 + bits + E)
+    lo = -(1 << (bits - 1))
+    codes = rng.integers(lo, -lo, size=(E, K, N), dtype=np.int64).astype(np.int8)
+    packed = np.stack([oracle.pack(codes[e], bits) for e in range(E)])
+    sbits = np.arange(0x7C00, dtype=np.uint16)                       # 0 .. largest finite
+    flat = np.concatenate([sbits, rng.integers(0x1000, 0x2000, size=E * K * (N // g) - sbits.size,
+                                               dtype=np.uint16)])
+    scales = flat[: E * K * (N // g)].reshape(E, K, N // g).view(np.float16)
+    ids = (np.arange(T) * E // T).astype(np.int32).reshape(T, 1)     # non-decreasing: permuted = token order
+    n_r = np.array([(r % (N // g)) * g + (37 * r) % g for r in range(T)])
+    h = np.zeros((T, N), np.uint16)
+    h[np.arange(T), n_r] = 0x3F80                                    # bf16 1.0
+    ws = moe.alloc_workspace(T, K, N, E, 1, bits)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    moe.route(dev(ids), E, K, N, bits, workspace=ws)
+    y = moe.w2(gu.dev_bf16(h), dev(packed), dev(scales), T=T, topk=1, bits=bits, group_size_w2=g, workspace=ws)
+    assert moe.read_status(ws) == moe.OK
+    got = gu.host_bits(y).astype(np.uint32)
+    deq = [oracle.dequant(packed[e], scales[e], N, g, bits) for e in range(E)]
+    want = np.stack([deq[ids[r, 0]][:, n_r[r]] for r in range(T)]).astype(np.uint32)
+    zero = lambda b: np.where((b & 0x7FFF) == 0, 0, b)              # +0 and -0 are the same weight
+    bad = np.argwhere(zero(got) != zero(want))
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])], want[tuple(bad[0])])

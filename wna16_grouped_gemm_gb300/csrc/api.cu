@@ -328,7 +328,7 @@ struct GemmPlan {
 
 int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uint16_t* wscales, const void* b_src,
               void* out, int64_t K, int64_t N, int64_t E, int group, float limit, const Layout& L, void* ws,
-              bool h_interleaved = false, const float* csum = nullptr) {
+              int h_interleaved = 0, const float* csum = nullptr) {
     DevInfo dev;
     if (int rc = device_info(dev)) return rc;
     const int64_t kred = w13 ? K : N;
@@ -415,9 +415,14 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.status = at<int>(ws, L.status);
     gp.ksplit = ksplit;
     gp.partial = ksplit > 1 ? at<float>(ws, L.partial) : nullptr;
+    // Prefill tiles: an expert's weights are read once per token tile of that
+    // expert, by CTAs running at about the same time, so they are kept in L2
+    // (evict-first made every tile re-read them from HBM); decode streams
+    // each weight once.
+    gp.w_reuse = nt >= 64 ? 1 : 0;
     gp.partial_rows = static_cast<int>(L.R);
     gp.n_weight_rows = E * rows_per_expert;
-    gp.h_interleaved = h_interleaved ? 1 : 0;
+    gp.h_interleaved = h_interleaved;
     // widest async copy that divides the scale row stride, one split's row
     // segment and the base alignment
     gp.scale_copy_bytes = 0;
@@ -536,9 +541,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     GemmPlan p13, p2;
-    // 2-bit weights are consumed in the interleaved 16-k order: x is gathered
-    // and h is written in that order (w2's input), y and out are not affected.
-    const bool il = bits == 2;
+    // The A operand's K order is interleaved (2-bit: 16-k blocks, 4-bit: 8-k
+    // words): x is gathered and h is written in that order (w2's input); y and
+    // out are not affected.
+    const int il = bits == 2 ? 1 : 2;
     // Group-accumulate mode takes offset codes when the token operand's
     // corrections are written with it: by the gather for w13, by the split-K
     // finalize (which writes h) for w2.
@@ -561,7 +567,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
                                       at<int>(workspace, L.offsets), at<int>(workspace, L.perm),
                                       at<int>(workspace, L.inv), at<int4>(workspace, L.tiles),
                                       at<int>(workspace, L.n_tiles), at<int>(workspace, L.status),
-                                      static_cast<const __nv_bfloat16*>(x), static_cast<int>(K), il ? 1 : 0,
+                                      static_cast<const __nv_bfloat16*>(x), static_cast<int>(K), il,
                                       at<__nv_bfloat16>(workspace, L.xp),
                                       p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
         if (e != cudaSuccess) return cuda_fail(e, "route/gather kernel launch");
@@ -573,7 +579,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
         mark(1, s);
         e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                           at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk, static_cast<int>(K),
-                          il ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
+                          il, at<__nv_bfloat16>(workspace, L.xp),
                           p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status), s);
         if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
         launches += 1;
@@ -582,7 +588,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
     if (int rc = launch_plan(p13, s)) return rc;
     if (p13.gp.ksplit > 1) {   // split K: fixed-order sum of the splits + SwiGLU -> h
         e = launch_finalize_w13(at<float>(workspace, L.partial), p13.gp.ksplit, static_cast<int>(L.R),
-                                at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, il ? 1 : 0,
+                                at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, il,
                                 at<__nv_bfloat16>(workspace, L.h), p2.gp.csum ? at<float>(workspace, L.csum2) : nullptr,
                                 s);
         if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
@@ -778,7 +784,7 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
     if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
     cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
-                                  static_cast<int>(K), bits == 2 ? 1 : 0, at<__nv_bfloat16>(workspace, L.xp),
+                                  static_cast<int>(K), bits == 2 ? 1 : 2, at<__nv_bfloat16>(workspace, L.xp),
                                   p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status),
                                   s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
@@ -807,8 +813,8 @@ int wna16_moe_w2(const void* h, const int32_t* w2_packed, const uint16_t* w2_sca
     if (int rc = check_workspace(workspace, workspace_bytes, L)) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const void* b_src = h;
-    if (bits == 2) {   // 2-bit weights read h in the interleaved 16-k order
-        cudaError_t e = launch_interleave_rows(static_cast<const __nv_bfloat16*>(h), L.R, N, 0,
+    {   // the weights read h in the A operand's interleaved K order
+        cudaError_t e = launch_interleave_rows(static_cast<const __nv_bfloat16*>(h), L.R, N, bits == 2 ? 1 : 2,
                                                at<__nv_bfloat16>(workspace, L.h), s);
         if (e != cudaSuccess) return cuda_fail(e, "interleave kernel launch");
         b_src = at<void>(workspace, L.h);

@@ -1,6 +1,6 @@
 // Exact WNA16 dequantisation helpers shared by the grouped GEMM kernels:
 // packed INT32 words of 2- or 4-bit codes -> BF16 pairs for the TMEM A operand,
-// plus the clamped SwiGLU and the interleaved 16-k order.
+// plus the clamped SwiGLU and the interleaved K orders.
 #pragma once
 
 #include <cstdint>
@@ -19,35 +19,10 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
     return d;
 }
 
-// 4-bit fields: a field q placed at mantissa bit `pos` of a float whose
-// exponent field is (150 - pos) reads as 2^(23-pos) + q.  fma(that, s,
-// -(2^(23-pos) + 8) * s) then equals (q - 8) * s = code * s EXACTLY: the
-// product has at most 4 + 11 significant bits and the offset constant at most
-// 13 + 11 <= 24 bits for the positions used (8, 12, 16), so the single
-// rounding of the FMA has nothing to round.  One cvt.rn.bf16x2 then gives the
-// correctly rounded BF16 weights.
-template <int POS>
-__device__ __forceinline__ uint32_t magic_bits() {
-    return static_cast<uint32_t>(150 - POS) << 23;
-}
-
-template <int BITS, int POS>
-__device__ __forceinline__ float field_value(uint32_t src, float s, float negoff) {
-    constexpr uint32_t mask = ((1u << BITS) - 1u) << POS;
-    const uint32_t b = and_or(src, mask, magic_bits<POS>());
-    return __fmaf_rn(__uint_as_float(b), s, negoff);
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
-
-// Constants -(2^(23-pos) + 8) * s for one scale (4-bit fields).
-struct Neg4 {  // 4-bit: pos 8, 12, 16
-    float c8, c12, c16;
-    __device__ __forceinline__ explicit Neg4(float s) : c8(-32776.0f * s), c12(-2056.0f * s), c16(-136.0f * s) {}
-};
 
 // 2-bit fields: in BF16, 0x4300 is 128.0
 // with a unit last place, so OR-ing a field q into mantissa bits 2i..2i+1
@@ -161,15 +136,39 @@ __device__ __forceinline__ void codes_chunk2(const uint8_t* row, uint32_t xr, in
     }
 }
 
-// One 4-bit word (8 consecutive k) -> 4 bf16x2.
-__device__ __forceinline__ void dequant_word4(uint32_t w, float s, const Neg4& c, uint32_t* o) {
-    const uint32_t a = w << 8;    // nibbles 0, 1 at bits 8, 12
-    const uint32_t m = w;         // nibbles 2, 3, 4 at bits 8, 12, 16
-    const uint32_t r = w >> 12;   // nibbles 5, 6, 7 at bits 8, 12, 16
-    o[0] = pack_bf16x2(field_value<4, 8>(a, s, c.c8), field_value<4, 12>(a, s, c.c12));
-    o[1] = pack_bf16x2(field_value<4, 8>(m, s, c.c8), field_value<4, 12>(m, s, c.c12));
-    o[2] = pack_bf16x2(field_value<4, 16>(m, s, c.c16), field_value<4, 8>(r, s, c.c8));
-    o[3] = pack_bf16x2(field_value<4, 12>(r, s, c.c12), field_value<4, 16>(r, s, c.c16));
+// 4-bit fields, exact: bf16_rne(code * s) for an fp16 scale s.  With
+// s_hi = bf16(s) and s_lo = s - s_hi (exact: an fp16 significand has 11 bits,
+// so s_lo is a multiple of s's fp16 ulp of magnitude at most 4 of them, at
+// most 2 significant bits), code * s = code * s_hi + code * s_lo exactly;
+// t = code * s_lo has at most 3 + 2 significant bits and is exact in BF16, and
+// one bf16x2 FMA code * s_hi + t rounds the exact sum once.  The code is read
+// exactly: a field q OR-ed into the low mantissa bits of 128.0 reads 128 + q,
+// and adding -136 gives q - 8.  Pair c of a word holds fields c and c + 4, so
+// within every 8-k word the A operand's K order is (0, 4, 1, 5, 2, 6, 3, 7);
+// the token operand is stored in that order too (gather kernel, w13
+// epilogue).  Checked against the fp32 product rounded once for every finite
+// fp16 scale and every code.
+struct Scale4 {  // (s_hi, s_hi) and (s_lo, s_lo) as bf16x2
+    uint32_t hi2, lo2;
+    __device__ __forceinline__ explicit Scale4(float s) {
+        const float hi = __bfloat162float(__float2bfloat16_rn(s));
+        const float lo = s - hi;
+        hi2 = pack_bf16x2(hi, hi);
+        lo2 = pack_bf16x2(lo, lo);
+    }
+};
+
+__device__ __forceinline__ uint32_t dequant_pair4(uint32_t fields, const Scale4& c) {
+    const uint32_t q = bf2_add(and_or(fields, 0x000F000Fu, kBf2Magic), kBf2Neg136);   // codes, exact
+    return bf2_fma(q, c.hi2, bf2_mul(q, c.lo2));
+}
+
+// One 4-bit word (8 consecutive k) -> 4 bf16x2 (fields (c, c + 4) in pair c).
+__device__ __forceinline__ void dequant_word4(uint32_t w, const Scale4& c, uint32_t* o) {
+    o[0] = dequant_pair4(w, c);
+    o[1] = dequant_pair4(w >> 4, c);
+    o[2] = dequant_pair4(w >> 8, c);
+    o[3] = dequant_pair4(w >> 12, c);
 }
 
 // 64 consecutive k of one row (one TMEM A buffer row) -> 32 bf16x2.
@@ -189,15 +188,15 @@ __device__ __forceinline__ void dequant_chunk(const uint8_t* row, uint32_t xr, i
         const uint32_t j0 = static_cast<uint32_t>(2 * chunk);
         const uint4 v0 = *reinterpret_cast<const uint4*>(row + ((j0 ^ xr) << 4));
         const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((j0 + 1) ^ xr) << 4));
-        const Neg4 c(s);
-        dequant_word4(v0.x, s, c, o + 0);
-        dequant_word4(v0.y, s, c, o + 4);
-        dequant_word4(v0.z, s, c, o + 8);
-        dequant_word4(v0.w, s, c, o + 12);
-        dequant_word4(v1.x, s, c, o + 16);
-        dequant_word4(v1.y, s, c, o + 20);
-        dequant_word4(v1.z, s, c, o + 24);
-        dequant_word4(v1.w, s, c, o + 28);
+        const Scale4 c(s);
+        dequant_word4(v0.x, c, o + 0);
+        dequant_word4(v0.y, c, o + 4);
+        dequant_word4(v0.z, c, o + 8);
+        dequant_word4(v0.w, c, o + 12);
+        dequant_word4(v1.x, c, o + 16);
+        dequant_word4(v1.y, c, o + 20);
+        dequant_word4(v1.z, c, o + 24);
+        dequant_word4(v1.w, c, o + 28);
     }
 }
 
@@ -219,15 +218,15 @@ __device__ __forceinline__ void dequant_chunk_g32(const uint8_t* row, uint32_t x
         const uint32_t j0 = static_cast<uint32_t>(2 * chunk);
         const uint4 v0 = *reinterpret_cast<const uint4*>(row + ((j0 ^ xr) << 4));
         const uint4 v1 = *reinterpret_cast<const uint4*>(row + (((j0 + 1) ^ xr) << 4));
-        const Neg4 ca(s_a), cb(s_b);
-        dequant_word4(v0.x, s_a, ca, o + 0);
-        dequant_word4(v0.y, s_a, ca, o + 4);
-        dequant_word4(v0.z, s_a, ca, o + 8);
-        dequant_word4(v0.w, s_a, ca, o + 12);
-        dequant_word4(v1.x, s_b, cb, o + 16);
-        dequant_word4(v1.y, s_b, cb, o + 20);
-        dequant_word4(v1.z, s_b, cb, o + 24);
-        dequant_word4(v1.w, s_b, cb, o + 28);
+        const Scale4 ca(s_a), cb(s_b);
+        dequant_word4(v0.x, ca, o + 0);
+        dequant_word4(v0.y, ca, o + 4);
+        dequant_word4(v0.z, ca, o + 8);
+        dequant_word4(v0.w, ca, o + 12);
+        dequant_word4(v1.x, cb, o + 16);
+        dequant_word4(v1.y, cb, o + 20);
+        dequant_word4(v1.z, cb, o + 24);
+        dequant_word4(v1.w, cb, o + 28);
     }
 }
 
@@ -240,11 +239,19 @@ __device__ __forceinline__ float swiglu(float g, float u, float L) {
     return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-// Position of element k in the interleaved K order (0, 8, 1, 9, ..., 7, 15)
-// of a 16-k block.
-__device__ __forceinline__ int interleave16(int k) {
-    const int e = k & 15;
-    return (k & ~15) | (e < 8 ? 2 * e : 2 * (e - 8) + 1);
+// Position of element k in the interleaved K order of the A operand: mode 1
+// (2-bit) (0, 8, 1, 9, ..., 7, 15) within each 16-k block, mode 2 (4-bit)
+// (0, 4, 1, 5, 2, 6, 3, 7) within each 8-k block, mode 0 the natural order.
+__device__ __forceinline__ int interleave_pos(int k, int mode) {
+    if (mode == 1) {
+        const int e = k & 15;
+        return (k & ~15) | (e < 8 ? 2 * e : 2 * (e - 8) + 1);
+    }
+    if (mode == 2) {
+        const int e = k & 7;
+        return (k & ~7) | (e < 4 ? 2 * e : 2 * (e - 4) + 1);
+    }
+    return k;
 }
 
 }  // namespace wna16

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();
+            const uint64_t pol_w = p.w_reuse ? policy_evict_normal() : policy_evict_first();
             const uint64_t pol_b = policy_evict_last();
             const uint32_t tx = static_cast<uint32_t>(2 * w_tile_bytes + b_stage_bytes);
             Ring st;
@@ -571,7 +571,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
             if constexpr (W13) {
                 // gate = block 0, up = block 1 of the same lane
                 const int n0 = mt * kRowsPerTile + row;
-                const int n = p.h_interleaved ? interleave16(n0) : n0;
+                const int n = interleave_pos(n0, p.h_interleaved);
                 for (int j0 = jbeg; j0 < rows; j0 += kEW) {
                     float g[kEW], uu[kEW];
                     load(j0, g, uu);
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
             }
             if constexpr (W13) {
                 const int n0 = mt * kRowsPerTile + row;
-                const int n = p.h_interleaved ? interleave16(n0) : n0;
+                const int n = interleave_pos(n0, p.h_interleaved);
 #pragma unroll
                 for (int i = 0; i < N; ++i)
                     if (i < rows && in_bounds(row0 + i < p.partial_rows && n < p.out_ld, p.status))

@@ -33,10 +33,13 @@ struct GemmParams {
     float limit;                // SwiGLU limit (w13 only)
     int* status;                // device status word
     int ksplit;                 // K splits per unit (1: no split)
+    int w_reuse;                // weight tiles are read again by the expert's other token tiles: load
+                                // them with the normal L2 policy instead of evict-first
     float* partial;             // split-K partial sums [ksplit][mt_count][partial_rows][256] fp32
     int partial_rows;           // rows of the permuted token order (R)
     int64_t n_weight_rows;      // E * rows_per_expert (bound of the scale rows, bounds-checked build)
-    int h_interleaved;          // w13: store h columns in the interleaved 16-k order (2-bit w2 input)
+    int h_interleaved;          // w13: h column order of w2's input: 0 natural, 1 / 2 the interleaved
+                                // 16-k / 8-k order of the 2-bit / 4-bit A operand (interleave_pos)
     int scale_copy_bytes;       // 16, 8 or 4: cp.async size for the scale rows; 0: plain loads
     const float* csum;          // GA mode with offset codes: per scale group and permuted token row,
                                 // sum_k w(k) b[row, k] with w(k) = 130, 34, 10, 130, 34, 10, 130, 34
@@ -89,15 +92,16 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
 // corrections of the gathered rows, csum[g * R + i] = sum over group g of w(k) x.
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
                           int K, int interleave, __nv_bfloat16* xp, float* csum, int* status, cudaStream_t stream);
-// dst[i, :] = src[i, :] with every 16-element block in the interleaved K order
-// (0, 8, 1, 9, ..., 7, 15) (or back, with inverse = 1).
-cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
+// dst[i, :] = src[i, :] in the A operand's interleaved K order: mode 1 (2-bit)
+// (0, 8, 1, 9, ..., 7, 15) in every 16-element block, mode 2 (4-bit)
+// (0, 4, 1, 5, 2, 6, 3, 7) in every 8-element block.
+cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int mode,
                                    __nv_bfloat16* dst, cudaStream_t stream);
 // out bf16 [T, K], or with f32_out the unrounded fp32 sums (partial output)
 cudaError_t launch_combine(const __nv_bfloat16* y, const float* weights, const int* inv, int T, int topk, int K,
                            void* out, bool f32_out, int R, int* status, cudaStream_t stream);
 // Split-K epilogues (partial sums [ksplit][mt][R][256] fp32, rows < offsets_end):
-//   h[r, n] = bf16(swiglu(sum_s gate, sum_s up)) (column n at its interleaved position if `interleave`),
+//   h[r, n] = bf16(swiglu(sum_s gate, sum_s up)) (column n at its position in K order `interleave`, 0-2),
 //   and with csum the offset-code corrections of h for w2 (group 128), csum[g * R + r]
 cudaError_t launch_finalize_w13(const float* partial, int ksplit, int R, const int* offsets_end, int N, float limit,
                                 int interleave, __nv_bfloat16* h, float* csum, cudaStream_t stream);

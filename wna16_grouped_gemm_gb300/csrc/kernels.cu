@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(256)
 }
 
 // 16 BF16 (elements 0..15 of a block, as two 8-element vectors) -> the
-// interleaved order (0, 8, 1, 9, ..., 7, 15), and back.
+// interleaved order (0, 8, 1, 9, ..., 7, 15) of the 2-bit A operand.
 __device__ __forceinline__ void interleave_block(const uint4& lo, const uint4& hi, uint4& a, uint4& b) {
     a.x = __byte_perm(lo.x, hi.x, 0x5410);  // lo0 hi0
     a.y = __byte_perm(lo.x, hi.x, 0x7632);  // lo1 hi1
@@ -341,15 +341,15 @@ __device__ __forceinline__ void interleave_block(const uint4& lo, const uint4& h
     b.z = __byte_perm(lo.w, hi.w, 0x5410);
     b.w = __byte_perm(lo.w, hi.w, 0x7632);
 }
-__device__ __forceinline__ void deinterleave_block(const uint4& a, const uint4& b, uint4& lo, uint4& hi) {
-    lo.x = __byte_perm(a.x, a.y, 0x5410);
-    hi.x = __byte_perm(a.x, a.y, 0x7632);
-    lo.y = __byte_perm(a.z, a.w, 0x5410);
-    hi.y = __byte_perm(a.z, a.w, 0x7632);
-    lo.z = __byte_perm(b.x, b.y, 0x5410);
-    hi.z = __byte_perm(b.x, b.y, 0x7632);
-    lo.w = __byte_perm(b.z, b.w, 0x5410);
-    hi.w = __byte_perm(b.z, b.w, 0x7632);
+// 8 BF16 (one 8-element vector) -> the interleaved order (0, 4, 1, 5, 2, 6, 3, 7)
+// of the 4-bit A operand.
+__device__ __forceinline__ uint4 interleave8(const uint4& v) {
+    uint4 a;
+    a.x = __byte_perm(v.x, v.z, 0x5410);  // 0 4
+    a.y = __byte_perm(v.x, v.z, 0x7632);  // 1 5
+    a.z = __byte_perm(v.y, v.w, 0x5410);  // 2 6
+    a.w = __byte_perm(v.y, v.w, 0x7632);  // 3 7
+    return a;
 }
 
 // Weight of element k in the offset-code correction of the grouped GEMM's
@@ -377,17 +377,19 @@ __device__ __forceinline__ float offset_sum16(const uint4& lo, const uint4& hi) 
     return s;
 }
 
-// Xp[i, :] = x[perm[i] / topk, :] for the valid rows i < offsets[E]
-// (optionally in the interleaved 16-k order); with csum (interleaved order
-// only) also csum[g * R + i] = sum over the 128-element group g of
-// offset_weight(k) x[k].
+// Xp[i, :] = x[perm[i] / topk, :] for the valid rows i < offsets[E], in the
+// K order of the A operand (interleave: 0 natural, 1 the 16-k order of 2-bit
+// weights, 2 the 8-k order of 4-bit ones); with csum (order 1 only) also
+// csum[g * R + i] = sum over the 128-element group g of offset_weight(k) x[k].
 // Copies token row t of x into permuted row i of xp (one CTA; see gather_kernel).
 __device__ __forceinline__ void gather_row(const uint4* __restrict__ x, int64_t t, int i, int R, int vec_per_row,
                                            int interleave, uint4* __restrict__ xp, float* __restrict__ csum) {
     const uint4* src = x + t * vec_per_row;
     uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
-    if (!interleave) {
+    if (interleave == 0) {
         for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
+    } else if (interleave == 2) {
+        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = interleave8(__ldg(src + v));
     } else {
         // every warp runs the same number of rounds (the shuffles need all
         // lanes); 8 consecutive threads hold one group's 16 vectors
@@ -507,15 +509,19 @@ __global__ void __launch_bounds__(kSmallRouteThreads)
     if (e >= 0 && rank_ok && xp) gather_row(x, f / topk, rank, R, vec_per_row, interleave, xp, csum);
 }
 
-__global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t blocks, int inverse,
+// Rows of BF16 into the A operand's K order (mode 1: 16-element blocks, 2:
+// 8-element vectors); one thread per 16 elements.
+__global__ void interleave_rows_kernel(const uint4* __restrict__ src, int64_t blocks, int mode,
                                        uint4* __restrict__ dst) {
     const int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (b >= blocks) return;
     uint4 a, c;
-    if (inverse)
-        deinterleave_block(src[2 * b], src[2 * b + 1], a, c);
-    else
+    if (mode == 2) {
+        a = interleave8(src[2 * b]);
+        c = interleave8(src[2 * b + 1]);
+    } else {
         interleave_block(src[2 * b], src[2 * b + 1], a, c);
+    }
     dst[2 * b] = a;
     dst[2 * b + 1] = c;
 }
@@ -604,9 +610,12 @@ __global__ void finalize_w13_kernel(const float* __restrict__ partial, int R, co
     for (int e = 0; e < 4; ++e) {
         const int n = n0 + e;
         int col = n;
-        if (interleave) {
+        if (interleave == 1) {
             const int b = n & 15;
             col = (n & ~15) | (b < 8 ? 2 * b : 2 * (b - 8) + 1);
+        } else if (interleave == 2) {
+            const int b = n & 7;
+            col = (n & ~7) | (b < 4 ? 2 * b : 2 * (b - 4) + 1);
         }
         const __nv_bfloat16 hv = __float2bfloat16_rn(swiglu_clamped(gs[e], us[e], L));
         hr[col] = hv;
@@ -774,7 +783,8 @@ cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_be
     if (e != cudaSuccess) return e;
     route_gather_small_kernel<<<R, kSmallRouteThreads, smem, stream>>>(
         ids, R, E, e_begin, E_total, nt, topk, counts, offsets, perm, inv, tiles, n_tiles, status,
-        reinterpret_cast<const uint4*>(x), K / 8, interleave, reinterpret_cast<uint4*>(xp), interleave ? csum : nullptr);
+        reinterpret_cast<const uint4*>(x), K / 8, interleave, reinterpret_cast<uint4*>(xp),
+        interleave == 1 ? csum : nullptr);
     return cudaGetLastError();
 }
 
@@ -784,17 +794,17 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* of
     const int vpr = K / 8;
     const int threads = vpr >= 256 ? 256 : 32;
     return launch_pdl(gather_kernel, dim3(R), dim3(threads), 0, stream, reinterpret_cast<const uint4*>(x), perm,
-                      offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp), interleave ? csum : nullptr,
-                      status);
+                      offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp),
+                      interleave == 1 ? csum : nullptr, status);
 }
 
-cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int inverse,
+cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int mode,
                                    __nv_bfloat16* dst, cudaStream_t stream) {
     const int64_t blocks = rows * cols / 16;
     if (blocks == 0) return cudaSuccess;
     const int threads = 256;
     interleave_rows_kernel<<<static_cast<unsigned>((blocks + threads - 1) / threads), threads, 0, stream>>>(
-        reinterpret_cast<const uint4*>(src), blocks, inverse, reinterpret_cast<uint4*>(dst));
+        reinterpret_cast<const uint4*>(src), blocks, mode, reinterpret_cast<uint4*>(dst));
     return cudaGetLastError();
 }
 
