@@ -325,11 +325,16 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
         } else if (lane == 0 && issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
-            const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
             Ring st, ab, acc;
             bool ok = true;
             bool issued = false;
             for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
+                // MMA N: the item's token rows rounded up to 16, not the whole
+                // tile (an expert's last tile is often far from full); the
+                // columns beyond are neither written nor read for this item
+                const int rows = p.tiles[(v / ksplit) / p.mt_count].z;
+                const uint32_t n_mma = static_cast<uint32_t>(min(nt, (rows + 15) & ~15));
+                const uint32_t idesc = idesc_bf16_f32(128, n_mma < 16u ? 16u : n_mma);
                 if (!mbar_wait_bounded(&accempty[acc.idx], acc.phase ^ 1u, abort_flag, status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + acc.idx * acc_set_cols + static_cast<uint32_t>(issuer * nt);
