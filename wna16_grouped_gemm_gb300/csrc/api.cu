@@ -121,6 +121,8 @@ struct Layout {
     size_t status = 0, n_tiles = 0, counts = 0, offsets = 0, perm = 0, inv = 0, tiles = 0, xp = 0, h = 0, y = 0;
     size_t chunks = 0;                    // chunked routing scratch: [chunks][E] + [chunks] ints
     size_t partial = 0;
+    size_t flags = 0;
+    int64_t n_flags = 0;
     size_t csum13 = 0, csum2 = 0;         // offset-code corrections (2-bit, 16-token tiles): [groups][R]
     size_t total = 0;
 };
@@ -152,6 +154,10 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     L.h = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * N);
     L.y = o;        o = align_up(o + sizeof(__nv_bfloat16) * L.R * K);
     L.partial = o;  o = align_up(o + sizeof(float) * partial_floats);
+    // per w13 unit: how many epilogue warps of its first K split have parked
+    // their sums (paired splits, see plan_gemm); zeroed by the gather kernels
+    L.n_flags = L.max_tiles * (N / 128);
+    L.flags = o;    o = align_up(o + sizeof(int) * L.n_flags);
     // group-accumulate mode (2-bit, 16-token tiles, group 128) with offset codes
     const bool ga = bits == 2 && L.nt == 16;
     L.csum13 = o;   o = align_up(o + (ga ? sizeof(float) * L.R * (K / 128) : 0));
@@ -423,6 +429,13 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     gp.partial_rows = static_cast<int>(L.R);
     gp.n_weight_rows = E * rows_per_expert;
     gp.h_interleaved = h_interleaved;
+    // Prefill w13 split in two (the accumulation cap): the CTAs 2i and 2i + 1
+    // of a launch with an even grid run the two splits of the same unit at the
+    // same time; the second one's epilogue adds the first one's parked sums
+    // (fresh in L2) to its own accumulator and writes h, so no finalize
+    // kernel runs.  Only odd CTAs wait, and only on even ones.
+    gp.fuse_splits = (w13 && ksplit == 2 && nt > 32) ? 1 : 0;
+    gp.unit_flags = at<int>(ws, L.flags);
     // widest async copy that divides the scale row stride, one split's row
     // segment and the base alignment
     gp.scale_copy_bytes = 0;
@@ -435,6 +448,8 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
 
     const int64_t max_items = max_units * ksplit;
     P.grid = static_cast<int>(max_items < dev.sms ? max_items : dev.sms);
+    if (gp.fuse_splits) P.grid &= ~1;   // split parity = CTA parity (max_items is even)
+    if (P.grid < 1) P.grid = 1;
     P.smem = sm.total;
     P.w13 = w13;
     P.bits = bits;
@@ -569,7 +584,8 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
                                       at<int>(workspace, L.n_tiles), at<int>(workspace, L.status),
                                       static_cast<const __nv_bfloat16*>(x), static_cast<int>(K), il,
                                       at<__nv_bfloat16>(workspace, L.xp),
-                                      p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, s);
+                                      p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr,
+                                      at<int>(workspace, L.flags), static_cast<int>(L.n_flags), s);
         if (e != cudaSuccess) return cuda_fail(e, "route/gather kernel launch");
         launches += 1;
         mark(1, s);
@@ -580,13 +596,14 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
         e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
                           at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk, static_cast<int>(K),
                           il, at<__nv_bfloat16>(workspace, L.xp),
-                          p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status), s);
+                          p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status),
+                          at<int>(workspace, L.flags), static_cast<int>(L.n_flags), s);
         if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
         launches += 1;
     }
     mark(2, s);
     if (int rc = launch_plan(p13, s)) return rc;
-    if (p13.gp.ksplit > 1) {   // split K: fixed-order sum of the splits + SwiGLU -> h
+    if (p13.gp.ksplit > 1 && !p13.gp.fuse_splits) {   // split K: fixed-order sum of the splits + SwiGLU -> h
         e = launch_finalize_w13(at<float>(workspace, L.partial), p13.gp.ksplit, static_cast<int>(L.R),
                                 at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, il,
                                 at<__nv_bfloat16>(workspace, L.h), p2.gp.csum ? at<float>(workspace, L.csum2) : nullptr,
@@ -607,7 +624,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     mark(5, s);
     mark_done();
-    g_launches = launches + 3 + (p13.gp.ksplit > 1 ? 1 : 0);   // + w13 (+ finalize), w2, combine
+    g_launches = launches + 3 + (p13.gp.ksplit > 1 && !p13.gp.fuse_splits ? 1 : 0);   // + w13 (+ finalize), w2, combine
     return WNA16_OK;
 }
 
@@ -786,10 +803,10 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
                                   at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
                                   static_cast<int>(K), bits == 2 ? 1 : 2, at<__nv_bfloat16>(workspace, L.xp),
                                   p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status),
-                                  s);
+                                  at<int>(workspace, L.flags), static_cast<int>(L.n_flags), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     if (int rc = launch_plan(p13, s)) return rc;
-    if (p13.gp.ksplit > 1) {
+    if (p13.gp.ksplit > 1 && !p13.gp.fuse_splits) {
         e = launch_finalize_w13(at<float>(workspace, L.partial), p13.gp.ksplit, static_cast<int>(L.R),
                                 at<int>(workspace, L.offsets) + E, static_cast<int>(N), swiglu_limit, 0,
                                 static_cast<__nv_bfloat16*>(h_out), nullptr, s);

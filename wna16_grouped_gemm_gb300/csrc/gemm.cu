@@ -603,6 +603,36 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 }
             }
         };
+        // Paired splits (fuse_splits), after this CTA parked split 1 of w13 unit
+        // (mt, tile) and released its accumulator: add the split-0 sums that
+        // the partner CTA's thread of the same warp and lane parked and this
+        // thread's own split-1 sums (the finalize kernel's order: split 0,
+        // then 1) and write h, off the issuers' path.
+        auto finish = [&](int mt, int rows_all, int row0) {
+            if constexpr (W13) {
+                const int jbeg = halves && helper ? nt / 2 : 0;
+                const int rows = halves && !helper ? min(rows_all, nt / 2) : rows_all;
+                const int64_t R_rows = p.partial_rows;
+                const float* q0 = p.partial + (static_cast<int64_t>(mt) * R_rows + row0) * (2 * kRowsPerTile) + row;
+                const float* q1 = q0 + static_cast<int64_t>(p.mt_count) * R_rows * (2 * kRowsPerTile);
+                const int n = interleave_pos(mt * kRowsPerTile + row, p.h_interleaved);
+                for (int j0 = jbeg; j0 < rows; j0 += kEW) {
+                    float g[kEW], uu[kEW];
+#pragma unroll
+                    for (int i = 0; i < kEW; ++i) {
+                        const bool ok = j0 + i < rows && in_bounds(row0 + j0 + i < R_rows, p.status);
+                        const int64_t o = static_cast<int64_t>(j0 + i) * (2 * kRowsPerTile);
+                        g[i] = ok ? __ldcg(q0 + o) + q1[o] : 0.0f;
+                        uu[i] = ok ? __ldcg(q0 + o + kRowsPerTile) + q1[o + kRowsPerTile] : 0.0f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < kEW; ++i)
+                        if (j0 + i < rows && in_bounds(row0 + j0 + i < R_rows && n < p.out_ld, p.status))
+                            p.out[static_cast<int64_t>(row0 + j0 + i) * p.out_ld + n] =
+                                __float2bfloat16_rn(swiglu(g[i], uu[i], L));
+                }
+            }
+        };
         // Same, from sums held in registers (columns 0..N-1).
         auto emit_regs = [&](int split, int mt, int rows, int row0, const auto& y0, const auto& y1) {
             constexpr int N = sizeof(y0) / sizeof(y0[0]);
@@ -763,7 +793,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 const uint32_t a0 = tmem + lane_base + acc.idx * acc_set_cols;   // issuer i at + i * nt
                 // every load of a column chunk is issued before the one wait
                 // (TMEM loads take hundreds of cycles to complete)
-                emit(split, u % p.mt_count, tile.z, tile.y, [&](int j0, float (&s0)[kEW], float (&s1)[kEW]) {
+                auto loader = [&](int j0, float (&s0)[kEW], float (&s1)[kEW]) {
                     if (nh == 1) {
                         uint32_t d0[kEW], d1[kEW];
                         if constexpr (kEW == 16) {
@@ -795,11 +825,42 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                             }
                         }
                     }
-                });
+                };
+                const bool fused = W13 && p.fuse_splits;
+                emit(split, u % p.mt_count, tile.z, tile.y, loader);
+                if (fused && split == 0) {
+                    // publish: every lane's stores, then one count per warp
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) atomicAdd(p.unit_flags + u, 1);
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&accempty[acc.idx]);
                 acc.next(nacc);
+                if (fused && split == 1) {
+                    // wait (bounded) until all epilogue warps of the split-0 CTA
+                    // have parked this unit's sums, then write h
+                    int okw = 1;
+                    if (lane == 0) {
+                        const uint64_t t0 = globaltimer_ns();
+                        while (ld_acquire_gpu(p.unit_flags + u) < 2 * kEpilogueWarps) {
+                            if (*abort_flag) {
+                                okw = 0;
+                                break;
+                            }
+                            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                                *abort_flag = 1;
+                                atomicExch(status, kStatusTimeout);
+                                okw = 0;
+                                break;
+                            }
+                            __nanosleep(64);
+                        }
+                    }
+                    if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+                    finish(u % p.mt_count, tile.z, tile.y);
+                }
             }
         }
     }

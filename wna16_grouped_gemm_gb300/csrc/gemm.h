@@ -33,6 +33,8 @@ struct GemmParams {
     float limit;                // SwiGLU limit (w13 only)
     int* status;                // device status word
     int ksplit;                 // K splits per unit (1: no split)
+    int fuse_splits;            // w13, 2 splits: CTA 2i + 1 (split 1) adds CTA 2i's parked split-0 sums and writes h
+    int* unit_flags;            // per unit: epilogue warps of split 0 that have parked their sums (zeroed per forward)
     int w_reuse;                // weight tiles are read again by the expert's other token tiles: load
                                 // them with the normal L2 policy instead of evict-first
     float* partial;             // split-K partial sums [ksplit][mt_count][partial_rows][256] fp32
@@ -83,15 +85,17 @@ constexpr int kSmallRouteMax = 512;
 cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int topk,
                                       int* counts, int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles,
                                       int* status, const __nv_bfloat16* x, int K, int interleave, __nv_bfloat16* xp,
-                                      float* csum, cudaStream_t stream);
+                                      float* csum, int* flags, int n_flags, cudaStream_t stream);
 // Router: ids/weights [T, k] from fp32 logits [T, E] (+ bias [E] or null);
 // 1 <= k <= min(E, 32), E <= 1024.
 cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
                               float* weights, cudaStream_t stream);
 // With csum (2-bit interleaved order only, group 128): also the offset-code
 // corrections of the gathered rows, csum[g * R + i] = sum over group g of w(k) x.
+// Both gathers also zero flags[0, n_flags) (the w13 GEMM's per-unit flags).
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
-                          int K, int interleave, __nv_bfloat16* xp, float* csum, int* status, cudaStream_t stream);
+                          int K, int interleave, __nv_bfloat16* xp, float* csum, int* status, int* flags, int n_flags,
+                          cudaStream_t stream);
 // dst[i, :] = src[i, :] in the A operand's interleaved K order: mode 1 (2-bit)
 // (0, 8, 1, 9, ..., 7, 15) in every 16-element block, mode 2 (4-bit)
 // (0, 4, 1, 5, 2, 6, 3, 7) in every 8-element block.

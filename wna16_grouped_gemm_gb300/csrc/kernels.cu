@@ -414,11 +414,18 @@ __device__ __forceinline__ void gather_row(const uint4* __restrict__ x, int64_t 
     }
 }
 
+// Zeroes the w13 GEMM's per-unit flags (paired K splits) before it runs.
+__device__ __forceinline__ void zero_flags(int* __restrict__ flags, int n_flags) {
+    for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n_flags; j += gridDim.x * blockDim.x) flags[j] = 0;
+}
+
 __global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
                               const int* __restrict__ offsets_end, int R, int topk, int vec_per_row, int interleave,
-                              uint4* __restrict__ xp, float* __restrict__ csum, int* __restrict__ status) {
+                              uint4* __restrict__ xp, float* __restrict__ csum, int* __restrict__ status,
+                              int* __restrict__ flags, int n_flags) {
     pdl_wait();
     pdl_trigger();
+    zero_flags(flags, n_flags);
     const int i = blockIdx.x;
     if (i >= *offsets_end) return;
     const int f = perm[i];
@@ -439,8 +446,9 @@ __global__ void __launch_bounds__(kSmallRouteThreads)
                               int topk, int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm,
                               int* __restrict__ inv, int4* __restrict__ tiles, int* __restrict__ n_tiles,
                               int* __restrict__ status, const uint4* __restrict__ x, int vec_per_row, int interleave,
-                              uint4* __restrict__ xp, float* __restrict__ csum) {
+                              uint4* __restrict__ xp, float* __restrict__ csum, int* __restrict__ flags, int n_flags) {
     extern __shared__ int sm[];
+    zero_flags(flags, n_flags);
     int* le = sm;                      // [R] local expert of each slot (-1: skipped or bad)
     int* cnt = sm + R;                 // [E] (CTA 0)
     __shared__ int red[kSmallRouteThreads / 32];
@@ -776,7 +784,7 @@ cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int
 cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int topk,
                                       int* counts, int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles,
                                       int* status, const __nv_bfloat16* x, int K, int interleave, __nv_bfloat16* xp,
-                                      float* csum, cudaStream_t stream) {
+                                      float* csum, int* flags, int n_flags, cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
     const int smem = (R + E) * static_cast<int>(sizeof(int));
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_gather_small_kernel), smem);
@@ -784,18 +792,19 @@ cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_be
     route_gather_small_kernel<<<R, kSmallRouteThreads, smem, stream>>>(
         ids, R, E, e_begin, E_total, nt, topk, counts, offsets, perm, inv, tiles, n_tiles, status,
         reinterpret_cast<const uint4*>(x), K / 8, interleave, reinterpret_cast<uint4*>(xp),
-        interleave == 1 ? csum : nullptr);
+        interleave == 1 ? csum : nullptr, flags, n_flags);
     return cudaGetLastError();
 }
 
 cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
-                          int interleave, __nv_bfloat16* xp, float* csum, int* status, cudaStream_t stream) {
+                          int interleave, __nv_bfloat16* xp, float* csum, int* status, int* flags, int n_flags,
+                          cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
     const int vpr = K / 8;
     const int threads = vpr >= 256 ? 256 : 32;
     return launch_pdl(gather_kernel, dim3(R), dim3(threads), 0, stream, reinterpret_cast<const uint4*>(x), perm,
                       offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp),
-                      interleave == 1 ? csum : nullptr, status);
+                      interleave == 1 ? csum : nullptr, status, flags, n_flags);
 }
 
 cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int mode,

@@ -161,6 +161,14 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t pa
     }
 }
 
+// Load with acquire semantics at GPU scope (a flag another CTA publishes after
+// its stores and a fence).
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- cp.async
 
 // Asynchronous global -> shared copy of 4, 8 or 16 bytes (both addresses aligned to the size).
