@@ -382,19 +382,21 @@ __device__ __forceinline__ float offset_sum16(const uint4& lo, const uint4& hi) 
 // weights, 2 the 8-k order of 4-bit ones); with csum (order 1 only) also
 // csum[g * R + i] = sum over the 128-element group g of offset_weight(k) x[k].
 // Copies token row t of x into permuted row i of xp (one CTA; see gather_kernel).
+// `tid` of `nthr` threads (whole warps) copy the row.
 __device__ __forceinline__ void gather_row(const uint4* __restrict__ x, int64_t t, int i, int R, int vec_per_row,
-                                           int interleave, uint4* __restrict__ xp, float* __restrict__ csum) {
+                                           int interleave, uint4* __restrict__ xp, float* __restrict__ csum, int tid,
+                                           int nthr) {
     const uint4* src = x + t * vec_per_row;
     uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
     if (interleave == 0) {
-        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = __ldg(src + v);
+        for (int v = tid; v < vec_per_row; v += nthr) dst[v] = __ldg(src + v);
     } else if (interleave == 2) {
-        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dst[v] = interleave8(__ldg(src + v));
+        for (int v = tid; v < vec_per_row; v += nthr) dst[v] = interleave8(__ldg(src + v));
     } else {
         // every warp runs the same number of rounds (the shuffles need all
         // lanes); 8 consecutive threads hold one group's 16 vectors
-        for (int base = 0; base < vec_per_row; base += 2 * blockDim.x) {
-            const int v = base + 2 * threadIdx.x;
+        for (int base = 0; base < vec_per_row; base += 2 * nthr) {
+            const int v = base + 2 * tid;
             float part = 0.0f;
             if (v < vec_per_row) {
                 const uint4 lo = __ldg(src + v), hi = __ldg(src + v + 1);
@@ -408,7 +410,7 @@ __device__ __forceinline__ void gather_row(const uint4* __restrict__ x, int64_t 
                 part += __shfl_xor_sync(0xffffffffu, part, 1);
                 part += __shfl_xor_sync(0xffffffffu, part, 2);
                 part += __shfl_xor_sync(0xffffffffu, part, 4);
-                if ((threadIdx.x & 7) == 0 && v < vec_per_row) csum[static_cast<int64_t>(v >> 4) * R + i] = part;
+                if ((tid & 7) == 0 && v < vec_per_row) csum[static_cast<int64_t>(v >> 4) * R + i] = part;
             }
         }
     }
@@ -419,18 +421,21 @@ __device__ __forceinline__ void zero_flags(int* __restrict__ flags, int n_flags)
     for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n_flags; j += gridDim.x * blockDim.x) flags[j] = 0;
 }
 
-__global__ void gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm,
-                              const int* __restrict__ offsets_end, int R, int topk, int vec_per_row, int interleave,
-                              uint4* __restrict__ xp, float* __restrict__ csum, int* __restrict__ status,
-                              int* __restrict__ flags, int n_flags) {
+// One warp per permuted row, kGatherRows rows per CTA.
+constexpr int kGatherRows = 8;
+
+__global__ void __launch_bounds__(32 * kGatherRows)
+    gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm, const int* __restrict__ offsets_end,
+                  int R, int topk, int vec_per_row, int interleave, uint4* __restrict__ xp, float* __restrict__ csum,
+                  int* __restrict__ status, int* __restrict__ flags, int n_flags) {
     pdl_wait();
     pdl_trigger();
     zero_flags(flags, n_flags);
-    const int i = blockIdx.x;
-    if (i >= *offsets_end) return;
+    const int i = blockIdx.x * kGatherRows + (threadIdx.x >> 5);
+    if (i >= *offsets_end) return;   // whole warps
     const int f = perm[i];
     if (!in_bounds(f >= 0 && f < R, status)) return;
-    gather_row(x, f / topk, i, R, vec_per_row, interleave, xp, csum);
+    gather_row(x, f / topk, i, R, vec_per_row, interleave, xp, csum, threadIdx.x & 31, 32);
 }
 
 // Routing lists and the gather in one kernel, for small batches (decode):
@@ -514,7 +519,7 @@ __global__ void __launch_bounds__(kSmallRouteThreads)
             *status = any_bad ? kStatusBadRouting : kStatusOk;
         }
     }
-    if (e >= 0 && rank_ok && xp) gather_row(x, f / topk, rank, R, vec_per_row, interleave, xp, csum);
+    if (e >= 0 && rank_ok && xp) gather_row(x, f / topk, rank, R, vec_per_row, interleave, xp, csum, threadIdx.x, blockDim.x);
 }
 
 // Rows of BF16 into the A operand's K order (mode 1: 16-element blocks, 2:
@@ -801,8 +806,8 @@ cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* of
                           cudaStream_t stream) {
     if (R == 0) return cudaSuccess;
     const int vpr = K / 8;
-    const int threads = vpr >= 256 ? 256 : 32;
-    return launch_pdl(gather_kernel, dim3(R), dim3(threads), 0, stream, reinterpret_cast<const uint4*>(x), perm,
+    return launch_pdl(gather_kernel, dim3((R + kGatherRows - 1) / kGatherRows), dim3(32 * kGatherRows), 0, stream,
+                      reinterpret_cast<const uint4*>(x), perm,
                       offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp),
                       interleave == 1 ? csum : nullptr, status, flags, n_flags);
 }
