@@ -370,8 +370,9 @@ def test_small_tiles_ragged(moe, oracle):
 @pytest.mark.parametrize("K,E", [(512, 8), (1024, 64)])
 def test_decode_tiles_with_9_to_16_rows(moe, oracle, K, E):
     """2-bit, 16-token tiles (at most 4 rows per expert on average) where a few
-    experts get 9..16 rows: the 16-column path of the group-accumulate
-    epilogue, without (K=512) and with (K=1024, E=64) split K."""
+    experts get 9..16 rows: the routing cuts such an expert into tiles of at
+    most 8 rows (the group-accumulate epilogue's register budget), without
+    (K=512) and with (K=1024, E=64) split K."""
     w = _small(T=16, K=K, N=256, E=E, topk=2, bits=2)
     inp = _inputs(w)
     ids = np.array([0] * 12 + [1] * 14 + [2, 3, 4, 5, 6, 7], np.int32)

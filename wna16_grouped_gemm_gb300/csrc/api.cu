@@ -116,6 +116,7 @@ int choose_split(int64_t max_units, int64_t kred, int kp, int group, int nt) {
 struct Layout {
     int64_t R = 0;
     int nt = 16;
+    int tile_rows = 16;
     int64_t max_tiles = 0;
     int64_t units13 = 0, units2 = 0;      // largest possible unit counts of the two GEMMs
     size_t status = 0, n_tiles = 0, counts = 0, offsets = 0, perm = 0, inv = 0, tiles = 0, xp = 0, h = 0, y = 0;
@@ -131,7 +132,11 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     Layout L;
     L.R = T * topk;
     L.nt = choose_nt(L.R, E);
-    L.max_tiles = (L.R < E ? L.R : E) + L.R / L.nt + 1;
+    // token rows per tile: nt, except 8 for 2-bit 16-token tiles (the
+    // group-accumulate epilogue keeps one fp32 sum per row and token, and
+    // 8 tokens fit its registers; an expert with more rows gets more tiles)
+    L.tile_rows = (bits == 2 && L.nt == 16) ? 8 : L.nt;
+    L.max_tiles = (L.R < E ? L.R : E) + L.R / L.tile_rows + 1;
     L.units13 = L.max_tiles * (N / 128);
     L.units2 = L.max_tiles * (K / 256);
     // split-K partial sums for the largest split any group size could give (32
@@ -313,7 +318,7 @@ int check_workspace(const void* ws, size_t bytes, const Layout& L) {
 int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStream_t s, int64_t e_begin = 0,
               int64_t E_total = -1) {
     cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), static_cast<int>(e_begin),
-                                 static_cast<int>(E_total < 0 ? E : E_total), L.nt, at<int>(ws, L.counts),
+                                 static_cast<int>(E_total < 0 ? E : E_total), L.tile_rows, at<int>(ws, L.counts),
                                  at<int>(ws, L.offsets), at<int>(ws, L.perm), at<int>(ws, L.inv),
                                  at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status),
                                  at<int>(ws, L.chunks), s);
@@ -578,7 +583,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
     if (L.R <= kSmallRouteMax) {
         // small batch: routing lists and gather in one kernel (the gather stage is folded into route)
         e = launch_route_gather_small(topk_ids, static_cast<int>(L.R), static_cast<int>(E), static_cast<int>(e_begin),
-                                      static_cast<int>(E_total), L.nt, topk, at<int>(workspace, L.counts),
+                                      static_cast<int>(E_total), L.tile_rows, topk, at<int>(workspace, L.counts),
                                       at<int>(workspace, L.offsets), at<int>(workspace, L.perm),
                                       at<int>(workspace, L.inv), at<int4>(workspace, L.tiles),
                                       at<int>(workspace, L.n_tiles), at<int>(workspace, L.status),

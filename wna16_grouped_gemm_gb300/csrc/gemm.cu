@@ -675,9 +675,8 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 // bf16(scale) * slot in group order.  For 2-bit codes (0 or +-2^j)
                 // code * bf16(scale) is exactly the BF16-rounded dequantised
                 // weight, so this is the same sum as with dequantised weights.
-                // Tiles of at most 8 tokens (every decode tile) read only 8
-                // columns per block.  With offset codes the slot holds
-                // sum (code + off + 2) x; the token's correction
+                // With offset codes the slot holds sum (code + off + 2) x; the
+                // token's correction
                 // sum (off + 2) x over the group (csum[group][permuted row]) is
                 // subtracted first, the same for both row blocks.
                 Ring sb, gs;   // gs: group slot ring (kGaSlots), advanced per group
@@ -695,89 +694,47 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                     const uint16_t* s1row = s0row + kRowsPerTile * ng_item;
                     // corrections of this item's groups for the tile's token rows
                     const float* crow = goff ? p.csum + static_cast<int64_t>(split * ng_item) * R_rows + tile.y : nullptr;
-                    if (tile.z <= 8) {
-                        float y0[8], y1[8];
+                    // tiles of 2-bit 16-token plans hold at most 8 token rows (the
+                    // routing cuts them so), which read 8 columns per block
+                    in_bounds(tile.z <= 8, status);
+                    float y0[8], y1[8];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) y0[i] = y1[i] = 0.0f;
-                        for (int g = 0; g < ng_item; ++g) {
-                            float cs[8];
+                    for (int i = 0; i < 8; ++i) y0[i] = y1[i] = 0.0f;
+                    for (int g = 0; g < ng_item; ++g) {
+                        float cs[8];
 #pragma unroll
-                            for (int i = 0; i < 8; ++i)
-                                cs[i] = goff && i < tile.z &&
-                                                in_bounds(tile.y + i < R_rows && split * ng_item + g < p.ngroups, status)
-                                            ? __ldg(crow + static_cast<int64_t>(g) * R_rows + i)
-                                            : 0.0f;
-                            if (!mbar_wait(&gfull[gs.idx], gs.phase, abort_flag, status)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            uint32_t d0[8], d1[8];
-                            const uint32_t col = gs.idx * (2 * 16);
-                            tc_ld_32x32b_x8(tmem + lane_base + col, d0);
-                            tc_ld_32x32b_x8(tmem + lane_base + col + 16, d1);
-                            tc_wait_ld();
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&gempty[gs.idx]);
-                            gs.next(kGaSlots);
-                            const float c0 = scale_of(s0row[g]);
-                            const float c1 = scale_of(s1row[g]);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                y0[i] = __fmaf_rn(c0, __uint_as_float(d0[i]) - cs[i], y0[i]);
-                                y1[i] = __fmaf_rn(c1, __uint_as_float(d1[i]) - cs[i], y1[i]);
-                            }
+                        for (int i = 0; i < 8; ++i)
+                            cs[i] = goff && i < tile.z &&
+                                            in_bounds(tile.y + i < R_rows && split * ng_item + g < p.ngroups, status)
+                                        ? __ldg(crow + static_cast<int64_t>(g) * R_rows + i)
+                                        : 0.0f;
+                        if (!mbar_wait(&gfull[gs.idx], gs.phase, abort_flag, status)) {
+                            ok = false;
+                            break;
                         }
-                        if (!ok) break;
+                        tc_fence_after();
+                        uint32_t d0[8], d1[8];
+                        const uint32_t col = gs.idx * (2 * 16);
+                        tc_ld_32x32b_x8(tmem + lane_base + col, d0);
+                        tc_ld_32x32b_x8(tmem + lane_base + col + 16, d1);
+                        tc_wait_ld();
+                        tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&sempty[sb.idx]);
-                        sb.next(2);
-                        emit_regs(split, u % p.mt_count, tile.z, tile.y, y0, y1);
-                    } else {
-                        float y0[16], y1[16];
+                        if (lane == 0) mbar_arrive(&gempty[gs.idx]);
+                        gs.next(kGaSlots);
+                        const float c0 = scale_of(s0row[g]);
+                        const float c1 = scale_of(s1row[g]);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) y0[i] = y1[i] = 0.0f;
-                        for (int g = 0; g < ng_item; ++g) {
-                            if (!mbar_wait(&gfull[gs.idx], gs.phase, abort_flag, status)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t col = gs.idx * (2 * 16);
-                            const float c0 = scale_of(s0row[g]);
-                            const float c1 = scale_of(s1row[g]);
-#pragma unroll
-                            for (int q = 0; q < 16; q += 8) {
-                                float cs[8];
-#pragma unroll
-                                for (int i = 0; i < 8; ++i)
-                                    cs[i] = goff && q + i < tile.z &&
-                                                    in_bounds(tile.y + q + i < R_rows &&
-                                                                  split * ng_item + g < p.ngroups, status)
-                                                ? __ldg(crow + static_cast<int64_t>(g) * R_rows + q + i)
-                                                : 0.0f;
-                                uint32_t d0[8], d1[8];
-                                tc_ld_32x32b_x8(tmem + lane_base + col + q, d0);
-                                tc_ld_32x32b_x8(tmem + lane_base + col + 16 + q, d1);
-                                tc_wait_ld();
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) {
-                                    y0[q + i] = __fmaf_rn(c0, __uint_as_float(d0[i]) - cs[i], y0[q + i]);
-                                    y1[q + i] = __fmaf_rn(c1, __uint_as_float(d1[i]) - cs[i], y1[q + i]);
-                                }
-                            }
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&gempty[gs.idx]);
-                            gs.next(kGaSlots);
+                        for (int i = 0; i < 8; ++i) {
+                            y0[i] = __fmaf_rn(c0, __uint_as_float(d0[i]) - cs[i], y0[i]);
+                            y1[i] = __fmaf_rn(c1, __uint_as_float(d1[i]) - cs[i], y1[i]);
                         }
-                        if (!ok) break;
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&sempty[sb.idx]);
-                        sb.next(2);
-                        emit_regs(split, u % p.mt_count, tile.z, tile.y, y0, y1);
                     }
+                    if (!ok) break;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sempty[sb.idx]);
+                    sb.next(2);
+                    emit_regs(split, u % p.mt_count, tile.z, tile.y, y0, y1);
                 }
             }
         } else {
