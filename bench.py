@@ -89,7 +89,7 @@ def load_peaks():
         sus, _ = pick("bf16_tflops_sustained")
         if hbm and bf16:
             return dict(hbm_gbs=hbm, bf16_tflops=bf16, bf16_tflops_sustained=sus,
-                        source="measured (MEASURED_PEAKS.json: hbm_gbs copy, bf16_tflops burst)")
+                        source="measured (MEASURED_PEAKS.json: hbm_gbs copy; bf16_tflops burst and bf16_tflops_sustained)")
     return dict(hbm_gbs=FALLBACK_HBM_GBS, bf16_tflops=FALLBACK_BF16_TFLOPS, bf16_tflops_sustained=None,
                 source="fallback (6800 GB/s, 1900 TFLOP/s)")
 
@@ -499,10 +499,21 @@ def measure(w, inp, args, dev, dist, rank, world):
                     frac=achieved / peaks["hbm_gbs"])
     else:
         achieved = facts[f"{dom}_flops"] / (dom_ms * 1e-3) / 1e12
-        roof = dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
-                    frac=achieved / peaks["bf16_tflops"])
-        if peaks.get("bf16_tflops_sustained"):
-            roof["frac_vs_sustained_peak"] = achieved / peaks["bf16_tflops_sustained"]
+        # The tensor peak for a kernel timed inside a seconds-long run of
+        # back-to-back forwards (the default sizing: ~1.5 s, under the power
+        # cap) is the sustained cuBLAS figure, measured the same way; a short
+        # timed region takes the burst figure.  The other fraction is kept too.
+        sus = peaks.get("bf16_tflops_sustained")
+        long_run = steps * ms >= 1000.0
+        if sus and long_run:
+            roof = dict(bound="tensor", achieved=achieved, peak=sus, unit="TFLOP/s", frac=achieved / sus,
+                        peak_kind="sustained (timed region of %.1f s)" % (steps * ms * 1e-3),
+                        frac_vs_burst_peak=achieved / peaks["bf16_tflops"])
+        else:
+            roof = dict(bound="tensor", achieved=achieved, peak=peaks["bf16_tflops"], unit="TFLOP/s",
+                        frac=achieved / peaks["bf16_tflops"], peak_kind="burst")
+            if sus:
+                roof["frac_vs_sustained_peak"] = achieved / sus
     roof.update(kernel=f"grouped_gemm_{dom}", peak_source=peaks["source"],
                 algorithmic_per_launch=facts[f"{dom}_kernel_bytes"] if decode else facts[f"{dom}_flops"],
                 algorithmic_unit="bytes" if decode else "flop", traffic=recorded_traffic(w.name, dom),
