@@ -38,6 +38,7 @@ CASES = {
     "w4_prefill_tiles_g64": _small(700, 1024, 512, 4, 2, 4, 128, 64),
     "w2_g32_tiles64": _small(96, 1024, 512, 4, 2, 2, 32, 32),
     "w4_chunked_route": _small(1200, 512, 256, 16, 8, 4, 128, 128),   # 9600 slots: routed by chunks
+    "w4_paired_k_splits": _small(300, 4096, 256, 3, 1, 4, 128, 128),  # w13 K splits on CTA pairs
 }
 
 

@@ -510,3 +510,16 @@ def test_dequant_exact_every_fp16_scale(moe, oracle, bits, E):
     zero = lambda b: np.where((b & 0x7FFF) == 0, 0, b)              # +0 and -0 are the same weight
     bad = np.argwhere(zero(got) != zero(want))
     assert bad.size == 0, (bad[:5], got[tuple(bad[0])], want[tuple(bad[0])])
+
+
+@pytest.mark.parametrize("bits,T,E", [(4, 300, 3), (2, 260, 2)])
+def test_paired_k_splits_small_grid(moe, oracle, bits, T, E):
+    """Prefill-sized tiles with K = 4096 (the w13 K range split in two, the
+    splits of a unit on CTA pairs, the second adding both and writing h) on a
+    grid far smaller than the SM count, with ragged expert tails; every
+    output against the oracle."""
+    w = _small(T=T, K=4096, N=256, E=E, topk=1, bits=bits)
+    ref, yb = _oracle_out_bound(oracle, w, _inputs(w))
+    out, status = _gpu_fwd(moe, w, gu.to_dev(_inputs(w)))
+    assert status == moe.OK
+    gu.assert_close(gu.host_bits(out), ref, f"paired splits bits={bits} T={T} E={E}", y_bound=yb)
