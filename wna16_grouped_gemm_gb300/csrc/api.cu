@@ -102,10 +102,13 @@ int min_split_for_chain(int nt, int64_t kred) {
     return S;
 }
 
-int choose_split(int64_t max_units, int64_t kred, int kp, int group, int nt) {
+// The w2 GEMM's splits are added by the combine, which reads ksplit x topk
+// partial rows per output, so its target stops at 4 splits (measured: 8 made
+// the one-token decode forward 4 % slower, the combine taking the extra).
+int choose_split(int64_t max_units, int64_t kred, int kp, int group, int nt, int max_split = 8) {
     int S = 1;
     const int need = min_split_for_chain(nt, kred);
-    while (S < 8 && (max_units * S < kTargetItems || S < need)) {
+    while (S < 8 && ((max_units * S < kTargetItems && S < max_split) || S < need)) {
         const int64_t next = 2 * S;
         if ((kred / kp) % next || (kred / next) % group) break;
         S = static_cast<int>(next);
@@ -142,7 +145,7 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     // split-K partial sums for the largest split any group size could give (32
     // is the smallest supported group): splits x row tiles x R token rows x 256
     const int64_t s13 = choose_split(L.units13, K, stage_k(L.nt, bits, K), 32, L.nt);
-    const int64_t s2 = choose_split(L.units2, N, stage_k(L.nt, bits, N), 32, L.nt);
+    const int64_t s2 = choose_split(L.units2, N, stage_k(L.nt, bits, N), 32, L.nt, 4);
     const int64_t p13 = s13 > 1 ? s13 * (N / 128) * L.R * 256 : 0;
     const int64_t p2 = s2 > 1 ? s2 * (K / 256) * L.R * 256 : 0;
     const int64_t partial_floats = p13 > p2 ? p13 : p2;
@@ -348,7 +351,7 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     const int kp = stage_k(nt, bits, kred);
     const int pitch = kp * bits / 8;
     const int64_t max_units = w13 ? L.units13 : L.units2;
-    const int ksplit = choose_split(max_units, kred, kp, group, nt);
+    const int ksplit = choose_split(max_units, kred, kp, group, nt, w13 ? 8 : 4);
     const int ngroups = static_cast<int>(kred / group);
     GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups / ksplit, dev.max_smem);
     if (sm.nstage < 2)
