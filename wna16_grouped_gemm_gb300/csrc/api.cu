@@ -434,6 +434,9 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     // (evict-first made every tile re-read them from HBM); decode streams
     // each weight once.
     gp.w_reuse = nt >= 64 ? 1 : 0;
+    // w2 reads the tile list written by the routing kernels, which ran before
+    // the w13 GEMM; only its token operand (h) comes from the kernel before it
+    gp.early_w = w13 ? 0 : 1;
     gp.partial_rows = static_cast<int>(L.R);
     gp.n_weight_rows = E * rows_per_expert;
     gp.h_interleaved = h_interleaved;

@@ -181,9 +181,17 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    // everything above overlapped the previous kernel; its outputs (tiles,
-    // token rows) are read only below
-    pdl_wait();
+    // Everything above overlapped the previous kernel; its outputs are read
+    // only below.  With early_w (the w2 GEMM, whose tile list was written
+    // kernels earlier) only the token tiles depend on the previous kernel: the
+    // producer issues the weights of its first stages before it waits, and
+    // the scale and dequant warps, which read only weights, scales and the
+    // tile list, start converting them without waiting; the issuers (token
+    // tiles) and the epilogue (which writes buffers the previous kernel may
+    // read) wait here.
+    const bool early_w = p.early_w != 0;
+    const bool is_dequant = warp >= kFirstDequantWarp && warp < kFirstDequantWarp + kDequantWarps;
+    if (!early_w || !(warp == kProducerWarp || warp == kScaleWarp || is_dequant)) pdl_wait();
     pdl_trigger();
 
     const int n_units = (*p.n_tiles) * p.mt_count;
@@ -213,6 +221,25 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
             Ring st;
             uint32_t issued = 0, last_parity = 0;   // per slot: issued at least once / parity of last issue
             bool ok = true;
+            // early_w: the weights of the first item's first stages (every slot
+            // is free at the start), then the dependency wait
+            int pre = 0;
+            if (early_w) {
+                if (static_cast<int>(blockIdx.x) < n_items) {
+                    const int u = static_cast<int>(blockIdx.x) / ksplit;
+                    const int split = static_cast<int>(blockIdx.x) - u * ksplit;
+                    const int4 tile = p.tiles[u / p.mt_count];
+                    int r0, r1;
+                    unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
+                    pre = min(nstage, kps);
+                    for (int i = 0; i < pre; ++i) {
+                        mbar_arrive_expect_tx(&full[i], tx);
+                        tma_load_3d(sW + i * 2 * w_tile_bytes, &tm_w, &full[i], (split * kps + i) * (kp / kCodes), r0,
+                                    0, pol_w);
+                    }
+                }
+                pdl_wait();
+            }
             for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
                 const int u = v / ksplit;
                 const int split = v - u * ksplit;
@@ -220,6 +247,15 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 int r0, r1;
                 unit_rows<W13>(p, tile.x, u % p.mt_count, r0, r1);
                 for (int ks = split * kps; ks < (split + 1) * kps; ++ks) {
+                    if (pre > 0 && v == static_cast<int>(blockIdx.x) && ks - split * kps < pre) {
+                        // weights already in flight: the token tile only
+                        tma_load_3d(sB + st.idx * b_stage_bytes, &tm_b, &full[st.idx], 0, tile.y, ks * (kp / 64),
+                                    pol_b);
+                        issued |= 1u << st.idx;
+                        last_parity = (last_parity & ~(1u << st.idx)) | (st.phase << st.idx);
+                        st.next(nstage);
+                        continue;
+                    }
                     if (!mbar_try_wait(smem_u32(&empty[st.idx]), st.phase ^ 1u) &&
                         !mbar_wait_bounded(&empty[st.idx], st.phase ^ 1u, abort_flag, status, true)) {
                         ok = false;

@@ -35,6 +35,8 @@ struct GemmParams {
     int ksplit;                 // K splits per unit (1: no split)
     int fuse_splits;            // w13, 2 splits: CTA 2i + 1 (split 1) adds CTA 2i's parked split-0 sums and writes h
     int* unit_flags;            // per unit: epilogue warps of split 0 that have parked their sums (zeroed per forward)
+    int early_w;                // the tile list is older than the previous kernel: weights of the first
+                                // stages are loaded and converted before the dependency wait
     int w_reuse;                // weight tiles are read again by the expert's other token tiles: load
                                 // them with the normal L2 policy instead of evict-first
     float* partial;             // split-K partial sums [ksplit][mt_count][partial_rows][256] fp32
