@@ -406,7 +406,6 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     // buffer parity) and large ones 2 (one per row block).  2-bit codes with
     // 16-token tiles take the group-accumulate mode: 6 issuers (row block x
     // group parity), 3 group slots of 32 columns, 3 A buffers.
-    gp.dequant_warps = 8;
     // group-accumulate mode: one A buffer per scale group (group == 128 k)
     gp.ga = (bits == 2 && nt == 16 && group == 128) ? 1 : 0;
     // offset codes when the caller provides the token corrections

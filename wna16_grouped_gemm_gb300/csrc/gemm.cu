@@ -901,7 +901,6 @@ static cudaError_t launch_impl(const CUtensorMap& tm_w, const CUtensorMap& tm_b,
 template <int BITS, bool W13>
 static cudaError_t launch_dw(const CUtensorMap& tm_w, const CUtensorMap& tm_b, const GemmParams& p, int grid,
                              int smem_bytes, cudaStream_t stream) {
-    if (p.dequant_warps != 8) return cudaErrorInvalidValue;
     if constexpr (BITS == 2) {
         if (p.ga && p.csum) return launch_impl<BITS, W13, 8, 2>(tm_w, tm_b, p, grid, smem_bytes, stream);
         if (p.ga) return launch_impl<BITS, W13, 8, 1>(tm_w, tm_b, p, grid, smem_bytes, stream);

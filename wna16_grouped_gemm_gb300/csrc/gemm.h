@@ -26,7 +26,6 @@ struct GemmParams {
     int nabuf;                  // TMEM A buffers (128 k each)
     int nacc;                   // TMEM accumulator sets (2: the epilogue overlaps the next item)
     int n_issuers;              // MMA-issuing threads (2, 4 or 6 in GA mode)
-    int dequant_warps;          // 8 or 16 (16: two warps per row block and lane quarter, alternate A buffers)
     int ga;                     // group-accumulate mode (2-bit codes, nt 16, group % 128 == 0): plain codes
                                 // into the MMA, one TMEM slot per scale group, scales applied by the epilogue
     int off_b, off_w, off_s, off_bar;   // smem layout (bytes from the 1024-aligned base)
