@@ -603,11 +603,10 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
         if (int rc = run_route(topk_ids, E, L, workspace, s, e_begin, E_total)) return rc;
         launches += route_chunks(static_cast<int>(L.R)) > 0 ? 3 : 1;
         mark(1, s);
-        e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
-                          at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk, static_cast<int>(K),
-                          il, at<__nv_bfloat16>(workspace, L.xp),
-                          p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status),
-                          at<int>(workspace, L.flags), static_cast<int>(L.n_flags), s);
+        e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.inv), static_cast<int>(T), topk,
+                          static_cast<int>(K), il, at<__nv_bfloat16>(workspace, L.xp),
+                          p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, static_cast<int>(L.R),
+                          at<int>(workspace, L.status), at<int>(workspace, L.flags), static_cast<int>(L.n_flags), s);
         if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
         launches += 1;
     }
@@ -809,11 +808,12 @@ int wna16_moe_w13(const void* x, const int32_t* topk_ids, const int32_t* w13_pac
                            group_size, swiglu_limit, L, workspace, false, at<float>(workspace, L.csum13)))
         return rc;
     if (int rc = run_route(topk_ids, E, L, workspace, s)) return rc;
-    cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.perm),
-                                  at<int>(workspace, L.offsets) + E, static_cast<int>(L.R), topk,
-                                  static_cast<int>(K), bits == 2 ? 1 : 2, at<__nv_bfloat16>(workspace, L.xp),
-                                  p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, at<int>(workspace, L.status),
-                                  at<int>(workspace, L.flags), static_cast<int>(L.n_flags), s);
+    cudaError_t e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.inv),
+                                  static_cast<int>(T), topk, static_cast<int>(K), bits == 2 ? 1 : 2,
+                                  at<__nv_bfloat16>(workspace, L.xp),
+                                  p13.gp.csum ? at<float>(workspace, L.csum13) : nullptr, static_cast<int>(L.R),
+                                  at<int>(workspace, L.status), at<int>(workspace, L.flags),
+                                  static_cast<int>(L.n_flags), s);
     if (e != cudaSuccess) return cuda_fail(e, "gather kernel launch");
     if (int rc = launch_plan(p13, s)) return rc;
     if (p13.gp.ksplit > 1 && !p13.gp.fuse_splits) {

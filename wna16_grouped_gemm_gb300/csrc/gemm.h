@@ -91,11 +91,13 @@ cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_be
 // 1 <= k <= min(E, 32), E <= 1024.
 cudaError_t launch_route_topk(const float* logits, const float* bias, int T, int E, int k, int32_t* ids,
                               float* weights, cudaStream_t stream);
+// Xp[inv[t * topk + j], :] = x[t, :] (in K order `interleave`) for every slot
+// of every token routed to a local expert (inv >= 0), one warp per token.
 // With csum (2-bit interleaved order only, group 128): also the offset-code
-// corrections of the gathered rows, csum[g * R + i] = sum over group g of w(k) x.
+// corrections of those rows, csum[g * R + i] = sum over group g of w(k) x.
 // Both gathers also zero flags[0, n_flags) (the w13 GEMM's per-unit flags).
-cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk,
-                          int K, int interleave, __nv_bfloat16* xp, float* csum, int* status, int* flags, int n_flags,
+cudaError_t launch_gather(const __nv_bfloat16* x, const int* inv, int T, int topk, int K, int interleave,
+                          __nv_bfloat16* xp, float* csum, int R, int* status, int* flags, int n_flags,
                           cudaStream_t stream);
 // dst[i, :] = src[i, :] in the A operand's interleaved K order: mode 1 (2-bit)
 // (0, 8, 1, 9, ..., 7, 15) in every 16-element block, mode 2 (4-bit)

@@ -404,29 +404,48 @@ __device__ __forceinline__ void gather_row(const uint4* __restrict__ x, int64_t 
                                            int nthr) {
     const uint4* src = x + t * vec_per_row;
     uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
-    if (interleave == 0) {
-        for (int v = tid; v < vec_per_row; v += nthr) dst[v] = __ldg(src + v);
-    } else if (interleave == 2) {
-        for (int v = tid; v < vec_per_row; v += nthr) dst[v] = interleave8(__ldg(src + v));
+    if (interleave != 1) {
+        // four loads in flight per thread before the stores
+        for (int v0 = tid; v0 < vec_per_row; v0 += 4 * nthr) {
+            uint4 a[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (v0 + j * nthr < vec_per_row) a[j] = __ldg(src + v0 + j * nthr);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (v0 + j * nthr < vec_per_row) dst[v0 + j * nthr] = interleave == 2 ? interleave8(a[j]) : a[j];
+        }
     } else {
         // every warp runs the same number of rounds (the shuffles need all
-        // lanes); 8 consecutive threads hold one group's 16 vectors
-        for (int base = 0; base < vec_per_row; base += 2 * nthr) {
-            const int v = base + 2 * tid;
-            float part = 0.0f;
-            if (v < vec_per_row) {
-                const uint4 lo = __ldg(src + v), hi = __ldg(src + v + 1);
-                uint4 a, b;
-                interleave_block(lo, hi, a, b);
-                dst[v] = a;
-                dst[v + 1] = b;
-                if (csum) part = offset_sum16(lo, hi);
+        // lanes); 8 consecutive threads hold one group's 16 vectors; two
+        // rounds' loads are in flight before their stores
+        for (int base = 0; base < vec_per_row; base += 4 * nthr) {
+            uint4 lo[2], hi[2];
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int v = base + r * 2 * nthr + 2 * tid;
+                if (v < vec_per_row) {
+                    lo[r] = __ldg(src + v);
+                    hi[r] = __ldg(src + v + 1);
+                }
             }
-            if (csum) {
-                part += __shfl_xor_sync(0xffffffffu, part, 1);
-                part += __shfl_xor_sync(0xffffffffu, part, 2);
-                part += __shfl_xor_sync(0xffffffffu, part, 4);
-                if ((tid & 7) == 0 && v < vec_per_row) csum[static_cast<int64_t>(v >> 4) * R + i] = part;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int v = base + r * 2 * nthr + 2 * tid;
+                float part = 0.0f;
+                if (v < vec_per_row) {
+                    uint4 a, b;
+                    interleave_block(lo[r], hi[r], a, b);
+                    dst[v] = a;
+                    dst[v + 1] = b;
+                    if (csum) part = offset_sum16(lo[r], hi[r]);
+                }
+                if (csum) {
+                    part += __shfl_xor_sync(0xffffffffu, part, 1);
+                    part += __shfl_xor_sync(0xffffffffu, part, 2);
+                    part += __shfl_xor_sync(0xffffffffu, part, 4);
+                    if ((tid & 7) == 0 && v < vec_per_row) csum[static_cast<int64_t>(v >> 4) * R + i] = part;
+                }
             }
         }
     }
@@ -437,21 +456,76 @@ __device__ __forceinline__ void zero_flags(int* __restrict__ flags, int n_flags)
     for (int j = blockIdx.x * blockDim.x + threadIdx.x; j < n_flags; j += gridDim.x * blockDim.x) flags[j] = 0;
 }
 
-// One warp per permuted row, kGatherRows rows per CTA.
+// One warp per token, kGatherRows tokens per CTA: the warp reads the token's
+// x row once and writes it (in the A operand's K order) to the permuted row
+// of each of its slots routed to a local expert (inv >= 0), with csum (order 1
+// only) also those rows' offset-code corrections.  Reading each x row once,
+// rather than once per slot, keeps the R = T * topk row writes from evicting
+// x from L2 between its reads.
 constexpr int kGatherRows = 8;
 
 __global__ void __launch_bounds__(32 * kGatherRows)
-    gather_kernel(const uint4* __restrict__ x, const int* __restrict__ perm, const int* __restrict__ offsets_end,
-                  int R, int topk, int vec_per_row, int interleave, uint4* __restrict__ xp, float* __restrict__ csum,
-                  int* __restrict__ status, int* __restrict__ flags, int n_flags) {
+    scatter_kernel(const uint4* __restrict__ x, const int* __restrict__ inv, int T, int topk, int vec_per_row,
+                   int interleave, uint4* __restrict__ xp, float* __restrict__ csum, int R, int* __restrict__ status,
+                   int* __restrict__ flags, int n_flags) {
     pdl_wait();
     pdl_trigger();
     zero_flags(flags, n_flags);
-    const int i = blockIdx.x * kGatherRows + (threadIdx.x >> 5);
-    if (i >= *offsets_end) return;   // whole warps
-    const int f = perm[i];
-    if (!in_bounds(f >= 0 && f < R, status)) return;
-    gather_row(x, f / topk, i, R, vec_per_row, interleave, xp, csum, threadIdx.x & 31, 32);
+    const int t = blockIdx.x * kGatherRows + (threadIdx.x >> 5);
+    if (t >= T) return;   // whole warps
+    const int lane = threadIdx.x & 31;
+    int mine = -1;        // lane j < topk: the permuted row of slot j (-1: not local)
+    if (lane < topk) {
+        const int r = inv[static_cast<int64_t>(t) * topk + lane];
+        mine = r >= 0 && in_bounds(r < R, status) ? r : -1;
+    }
+    const uint4* src = x + static_cast<int64_t>(t) * vec_per_row;
+    if (interleave != 1) {
+        // vec_per_row is a multiple of 32, so every lane runs the same rounds
+        for (int v0 = lane; v0 < vec_per_row; v0 += 4 * 32) {
+            uint4 a[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                if (v0 + c * 32 < vec_per_row) {
+                    a[c] = __ldg(src + v0 + c * 32);
+                    if (interleave == 2) a[c] = interleave8(a[c]);
+                }
+            for (int j = 0; j < topk; ++j) {
+                const int i = __shfl_sync(0xffffffffu, mine, j);
+                if (i < 0) continue;
+                uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    if (v0 + c * 32 < vec_per_row) dst[v0 + c * 32] = a[c];
+            }
+        }
+    } else {
+        // two vectors (one 16-element block) per lane and round; 8 consecutive
+        // lanes hold one 128-element group
+        for (int base = 0; base < vec_per_row; base += 2 * 32) {
+            const int v = base + 2 * lane;
+            uint4 a = make_uint4(0, 0, 0, 0), b = a;
+            float part = 0.0f;
+            if (v < vec_per_row) {
+                const uint4 lo = __ldg(src + v), hi = __ldg(src + v + 1);
+                interleave_block(lo, hi, a, b);
+                if (csum) part = offset_sum16(lo, hi);
+            }
+            if (csum) {
+                part += __shfl_xor_sync(0xffffffffu, part, 1);
+                part += __shfl_xor_sync(0xffffffffu, part, 2);
+                part += __shfl_xor_sync(0xffffffffu, part, 4);
+            }
+            for (int j = 0; j < topk; ++j) {
+                const int i = __shfl_sync(0xffffffffu, mine, j);
+                if (i < 0 || v >= vec_per_row) continue;
+                uint4* dst = xp + static_cast<int64_t>(i) * vec_per_row;
+                dst[v] = a;
+                dst[v + 1] = b;
+                if (csum && (lane & 7) == 0) csum[static_cast<int64_t>(v >> 4) * R + i] = part;
+            }
+        }
+    }
 }
 
 // Routing lists and the gather in one kernel, for small batches (decode):
@@ -567,17 +641,34 @@ __global__ void combine_kernel(const uint4* __restrict__ y, const float* __restr
     const int v = blockIdx.y * blockDim.x + threadIdx.x;
     if (v >= vec_per_row) return;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < topk; ++j) {
-        const int r = inv[t * topk + j];
-        if (r < 0 || !in_bounds(r < R, status)) continue;
-        const float wj = w[t * topk + j];
-        const uint4 q = __ldg(y + static_cast<int64_t>(r) * vec_per_row + v);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+    // up to 8 slots' rows in flight before the adds, which stay in slot order
+    for (int j0 = 0; j0 < topk; j0 += 8) {
+        uint4 q[8];
+        float wj[8];
+        bool ok[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(h[i]);
-            acc[2 * i] = __fmaf_rn(wj, f.x, acc[2 * i]);
-            acc[2 * i + 1] = __fmaf_rn(wj, f.y, acc[2 * i + 1]);
+        for (int c = 0; c < 8; ++c) {
+            const int j = j0 + c;
+            ok[c] = false;
+            if (j < topk) {
+                const int r = inv[t * topk + j];
+                ok[c] = r >= 0 && in_bounds(r < R, status);
+                if (ok[c]) {
+                    wj[c] = w[t * topk + j];
+                    q[c] = __ldg(y + static_cast<int64_t>(r) * vec_per_row + v);
+                }
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            if (!ok[c]) continue;
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q[c]);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(h[i]);
+                acc[2 * i] = __fmaf_rn(wj[c], f.x, acc[2 * i]);
+                acc[2 * i + 1] = __fmaf_rn(wj[c], f.y, acc[2 * i + 1]);
+            }
         }
     }
     if constexpr (F32OUT) {
@@ -817,15 +908,14 @@ cudaError_t launch_route_gather_small(const int32_t* ids, int R, int E, int e_be
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const __nv_bfloat16* x, const int* perm, const int* offsets_end, int R, int topk, int K,
-                          int interleave, __nv_bfloat16* xp, float* csum, int* status, int* flags, int n_flags,
+cudaError_t launch_gather(const __nv_bfloat16* x, const int* inv, int T, int topk, int K, int interleave,
+                          __nv_bfloat16* xp, float* csum, int R, int* status, int* flags, int n_flags,
                           cudaStream_t stream) {
-    if (R == 0) return cudaSuccess;
+    if (T == 0) return cudaSuccess;
     const int vpr = K / 8;
-    return launch_pdl(gather_kernel, dim3((R + kGatherRows - 1) / kGatherRows), dim3(32 * kGatherRows), 0, stream,
-                      reinterpret_cast<const uint4*>(x), perm,
-                      offsets_end, R, topk, vpr, interleave, reinterpret_cast<uint4*>(xp),
-                      interleave == 1 ? csum : nullptr, status, flags, n_flags);
+    return launch_pdl(scatter_kernel, dim3((T + kGatherRows - 1) / kGatherRows), dim3(32 * kGatherRows), 0, stream,
+                      reinterpret_cast<const uint4*>(x), inv, T, topk, vpr, interleave, reinterpret_cast<uint4*>(xp),
+                      interleave == 1 ? csum : nullptr, R, status, flags, n_flags);
 }
 
 cudaError_t launch_interleave_rows(const __nv_bfloat16* src, int64_t rows, int64_t cols, int mode,
