@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);   // warp-uniform
     // Everything above overlapped the previous kernel; its outputs are read
     // only below.  With early_w (the w2 GEMM, whose tile list was written
     // kernels earlier) only the token tiles depend on the previous kernel: the
@@ -297,8 +297,29 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
         // h = i >> 1 takes the groups g with g % 3 == h, and every group is
         // accumulated from zero into a slot of kGaSlots that the epilogue warps
         // scale and add up.
+        // The whole warp runs the loop: lane 0 waits and the warp follows its
+        // verdict; one elected thread issues each A buffer's MMAs and their
+        // commits (elect.sync keeps the operands in uniform registers, which
+        // makes each MMA ~3x cheaper to issue than under `if (lane == 0)`).
+        auto warp_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+            bool r = true;
+            if (lane == 0) r = mbar_wait(bar, parity, abort_flag, status);
+            return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+        };
+        // after a failure: no MMA of this issuer may still run when TMEM is released
+        auto drain_issuer = [&]() {
+            if (elect_one(status)) {
+                tc_commit(&drain[issuer]);
+                const uint32_t a = smem_u32(&drain[issuer]);
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(a, 0)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+                }
+            }
+            __syncwarp();
+        };
         if constexpr (ga) {
-          if (lane == 0 && issuer < n_iss) {
+          if (issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
             const uint32_t idesc = idesc_bf16_f32(128, static_cast<uint32_t>(nt));
@@ -306,8 +327,8 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
             // counted over all items, group g going to parity g % 3, so this
             // issuer's groups all use group slot h and A buffer h, and the
             // k-th of them waits for phase k of those barriers.  Counters
-            // instead of divisions: a single thread pays every instruction's
-            // full latency.
+            // instead of divisions: the issuing thread pays every
+            // instruction's full latency.
             uint32_t par = 0;    // parity of the current group
             uint32_t own = 0;    // groups of this parity issued so far
             const uint32_t d = tmem + static_cast<uint32_t>(h) * (2 * 16) + static_cast<uint32_t>(t * 16);
@@ -317,48 +338,44 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
             bool issued = false;
             for (int v = blockIdx.x; v < n_items && ok; v += gridDim.x) {
                 for (int ks = 0; ks < kps && ok; ++ks) {
-                    if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
+                    if (!warp_wait(&full[st.idx], st.phase)) {
                         ok = false;
                         break;
                     }
                     const uint32_t blo = smem_desc_sw128_lo(smem_u32(sB + st.idx * b_stage_bytes));
                     for (int c = 0; c < chunks; ++c) {
                         if (par == static_cast<uint32_t>(h)) {
-                            if (!mbar_wait(&gempty[h], (own & 1u) ^ 1u, abort_flag, status) ||
-                                !mbar_wait(&afull[h * 2 + t], own & 1u, abort_flag, status)) {
+                            if (!warp_wait(&gempty[h], (own & 1u) ^ 1u) || !warp_wait(&afull[h * 2 + t], own & 1u)) {
                                 ok = false;
                                 break;
                             }
-                            tc_fence_after();
                             // B: 64-k swizzle atoms 2c and 2c+1, 32 B per 16 k inside each
                             const uint32_t lo0 = blo + static_cast<uint32_t>(2 * c) * nt8;
                             const uint32_t lo1 = lo0 + nt8;
+                            if (elect_one(status)) {
+                                tc_fence_after();
 #pragma unroll
-                            for (int k16 = 0; k16 < 8; ++k16)
-                                tc_mma_ts_lohi(d, a0 + k16 * 8, (k16 < 4 ? lo0 : lo1) + (k16 & 3) * 2, kSmemDescSw128Hi,
-                                               idesc, k16 == 0 ? 0u : 1u);
+                                for (int k16 = 0; k16 < 8; ++k16)
+                                    tc_mma_ts_lohi(d, a0 + k16 * 8, (k16 < 4 ? lo0 : lo1) + (k16 & 3) * 2,
+                                                   kSmemDescSw128Hi, idesc, k16 == 0 ? 0u : 1u);
+                                tc_commit(&aempty[h * 2 + t]);
+                                tc_commit(&gfull[h]);
+                            }
+                            __syncwarp();
                             issued = true;
-                            tc_commit(&aempty[h * 2 + t]);
-                            tc_commit(&gfull[h]);
                             ++own;
                         }
                         par = par == 2u ? 0u : par + 1u;
                     }
                     if (!ok) break;
-                    tc_commit(&empty[st.idx]);
+                    if (elect_one(status)) tc_commit(&empty[st.idx]);
+                    __syncwarp();
                     st.next(nstage);
                 }
             }
-            if (!ok && issued) {
-                tc_commit(&drain[issuer]);
-                const uint32_t a = smem_u32(&drain[issuer]);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(a, 0)) {
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-                }
-            }
+            if (!ok && issued) drain_issuer();
           }
-        } else if (lane == 0 && issuer < n_iss) {
+        } else if (issuer < n_iss) {
             const int t = issuer & 1;
             const int h = issuer >> 1;
             Ring st, ab, acc;
@@ -368,59 +385,54 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 // MMA N: the item's token rows rounded up to 16, not the whole
                 // tile (an expert's last tile is often far from full); the
                 // columns beyond are neither written nor read for this item
-                const int rows = p.tiles[(v / ksplit) / p.mt_count].z;
+                const int rows = __shfl_sync(0xffffffffu, p.tiles[(v / ksplit) / p.mt_count].z, 0);
                 const uint32_t n_mma = static_cast<uint32_t>(min(nt, (rows + 15) & ~15));
                 const uint32_t idesc = idesc_bf16_f32(128, n_mma < 16u ? 16u : n_mma);
-                if (!mbar_wait_bounded(&accempty[acc.idx], acc.phase ^ 1u, abort_flag, status)) break;
-                tc_fence_after();
+                if (!warp_wait(&accempty[acc.idx], acc.phase ^ 1u)) break;
                 const uint32_t d = tmem + acc.idx * acc_set_cols + static_cast<uint32_t>(issuer * nt);
                 uint32_t accumulate = 0;
                 int bl = 0;   // A buffer index within the item
                 for (int ks = 0; ks < kps && ok; ++ks) {
-                    if (!mbar_wait(&full[st.idx], st.phase, abort_flag, status)) {
+                    if (!warp_wait(&full[st.idx], st.phase)) {
                         ok = false;
                         break;
                     }
                     const uint32_t blo = smem_desc_sw128_lo(smem_u32(sB + st.idx * b_stage_bytes));
                     for (int c = 0; c < chunks; ++c, ++bl) {
                         if (n_iss == 2 || (bl & 1) == h) {
-                            if (!mbar_wait(&afull[ab.idx * 2 + t], ab.phase, abort_flag, status)) {
+                            if (!warp_wait(&afull[ab.idx * 2 + t], ab.phase)) {
                                 ok = false;
                                 break;
                             }
-                            tc_fence_after();
                             const uint32_t a0 = tmem + abase_col + ab.idx * 128 + t * 64;
                             // B: 64-k swizzle atoms 2c and 2c+1, 32 B per 16 k inside each
                             const uint32_t lo0 = blo + static_cast<uint32_t>(2 * c) * nt8;
                             const uint32_t lo1 = lo0 + nt8;
+                            if (elect_one(status)) {
+                                tc_fence_after();
 #pragma unroll
-                            for (int k16 = 0; k16 < 8; ++k16) {
-                                tc_mma_ts_lohi(d, a0 + k16 * 8, (k16 < 4 ? lo0 : lo1) + (k16 & 3) * 2, kSmemDescSw128Hi,
-                                               idesc, accumulate);
-                                accumulate = 1;
+                                for (int k16 = 0; k16 < 8; ++k16)
+                                    tc_mma_ts_lohi(d, a0 + k16 * 8, (k16 < 4 ? lo0 : lo1) + (k16 & 3) * 2,
+                                                   kSmemDescSw128Hi, idesc, (accumulate | k16) != 0 ? 1u : 0u);
+                                tc_commit(&aempty[ab.idx * 2 + t]);
                             }
+                            __syncwarp();
+                            accumulate = 1;
                             issued = true;
-                            tc_commit(&aempty[ab.idx * 2 + t]);
                         }
                         ab.next(nabuf);
                     }
                     if (!ok) break;
-                    tc_commit(&empty[st.idx]);
+                    if (elect_one(status)) tc_commit(&empty[st.idx]);
+                    __syncwarp();
                     st.next(nstage);
                 }
                 if (!ok) break;
-                tc_commit(&accfull[acc.idx]);
+                if (elect_one(status)) tc_commit(&accfull[acc.idx]);
+                __syncwarp();
                 acc.next(nacc);
             }
-            if (!ok && issued) {
-                // make sure no MMA of this issuer is still running before TMEM is released
-                tc_commit(&drain[issuer]);
-                const uint32_t a = smem_u32(&drain[issuer]);
-                const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(a, 0)) {
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-                }
-            }
+            if (!ok && issued) drain_issuer();
         }
     } else if (warp == kScaleWarp) {
         // ------------------------------------------------------------ scale loader

@@ -62,7 +62,33 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31) == 0; }
+// One thread of a converged warp (elect.sync over all 32 lanes; with every
+// lane active it is the same lane each time, so a later commit is issued by
+// the thread that issued the MMAs it tracks).  Measured on the GB300: eight
+// tcgen05.mma + commit issued inside such a block take ~210-350 cycles, the
+// same instructions under `if (lane == 0)` ~650-670 (their operands then go
+// through per-thread registers).  The bounds-checked build records
+// kStatusIndex if the elected lane is ever not lane 0.
+__device__ __forceinline__ bool elect_one(int* status) {
+    uint32_t pred;
+#ifdef WNA16_DEBUG
+    uint32_t leader;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "elect.sync %0|q, 0xffffffff;\n\t"
+        "selp.u32 %1, 1, 0, q;\n\t}"
+        : "=r"(leader), "=r"(pred));
+    if (pred && leader != 0) atomicExch(status, kStatusIndex);
+#else
+    (void)status;
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "elect.sync _|q, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(pred));
+#endif
+    return pred != 0;
+}
 
 // ---------------------------------------------------------------- programmatic dependent launch
 
