@@ -833,16 +833,18 @@ __global__ void __launch_bounds__(Roles<DW>::kThreads, 1)
                 };
                 const bool fused = W13 && p.fuse_splits;
                 emit(split, u % p.mt_count, tile.z, tile.y, loader);
+                // the accumulator is free once its loads have landed in
+                // registers: release it before the stores are made visible
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[acc.idx]);
+                acc.next(nacc);
                 if (fused && split == 0) {
                     // publish: every lane's stores, then one count per warp
                     __threadfence();
                     __syncwarp();
                     if (lane == 0) atomicAdd(p.unit_flags + u, 1);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&accempty[acc.idx]);
-                acc.next(nacc);
                 if (fused && split == 1) {
                     // wait (bounded) until all epilogue warps of the split-0 CTA
                     // have parked this unit's sums, then write h
