@@ -25,9 +25,10 @@ def libs():
     return moe, moe.load_library(), binding.load_debug_library()
 
 
-def _small(T, K, N, E, topk, bits, g13, g2):
+def _small(T, K, N, E, topk, bits, g13, g2, zipf=0.0):
     return synth.Workload("dbg", T=T, K=K, N=N, E=E, topk=topk, bits=bits, g13=g13, g2=g2,
-                          scale_lo=0.005 if bits == 2 else 0.001, scale_hi=0.02 if bits == 2 else 0.005)
+                          scale_lo=0.005 if bits == 2 else 0.001, scale_hi=0.02 if bits == 2 else 0.005,
+                          zipf_s=zipf)
 
 
 CASES = {
@@ -39,6 +40,8 @@ CASES = {
     "w2_g32_tiles64": _small(96, 1024, 512, 4, 2, 2, 32, 32),
     "w4_chunked_route": _small(1200, 512, 256, 16, 8, 4, 128, 128),   # 9600 slots: routed by chunks
     "w4_paired_k_splits": _small(300, 4096, 256, 3, 1, 4, 128, 128),  # w13 K splits on CTA pairs
+    "w2_light_experts": _small(1024, 4096, 512, 64, 4, 2, 128, 128, zipf=1.1),          # light-expert launches
+    "w2_light_experts_chunked": _small(2200, 4096, 512, 64, 4, 2, 128, 128, zipf=1.1),  # ... chunked routing
 }
 
 

@@ -289,6 +289,25 @@ def test_moderate_prefill_tiles_all_tokens(moe, oracle, bits, g13, g2, zipf):
     _check_all_tokens(moe, oracle, w, _inputs(w), f"moderate prefill bits={bits} g={g13}/{g2} zipf={zipf}")
 
 
+@pytest.mark.parametrize("T", [1024, 2200])
+def test_light_expert_launches(moe, oracle, T):
+    """2-bit prefill batches with a Zipf-skewed tail: experts with at most 8
+    rows run in their own group-accumulate launches over one tile each (two
+    more launches), the others in 128-token tiles; every output against the
+    oracle, with the single-CTA routing (4096 slots) and the chunked one
+    (8800 slots); hidden 4096, so that the main w2 GEMM runs unsplit (the light
+    path needs it to write y itself)."""
+    w = _small(T=T, K=4096, N=512, E=64, topk=4, bits=2, g13=128, g2=128, zipf=1.1, name="light")
+    inp = _inputs(w)
+    counts = np.bincount(np.asarray(inp["ids"]).reshape(-1), minlength=w.E)
+    assert ((counts > 0) & (counts <= 8)).sum() > 0 and (counts > 8).sum() > 0, counts
+    _check_all_tokens(moe, oracle, w, inp, f"light experts T={T}")
+    # route (three kernels when chunked), gather, w13 (+ its split-K finalize),
+    # light w13, w2, light w2, combine
+    from wna16_grouped_gemm_gb300 import binding
+    assert binding.launches_last_forward() >= (3 if w.R > 8192 else 1) + 6
+
+
 def _exact_rows_ids(E, topk, r):
     """ids with exactly r rows on each of E experts (T = E*r/topk tokens, each
     token's experts distinct)."""

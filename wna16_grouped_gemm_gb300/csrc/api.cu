@@ -61,6 +61,10 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
 // Token tile (MMA N) from the mean rows per expert.
+constexpr int kLightRows = 8;   // light experts: at most this many rows (one 8-row tile; measured
+                                // 1.3 % faster on the 2-bit Zipf prefill than 16, whose 9-16-row
+                                // experts took two light tiles)
+
 int choose_nt(int64_t R, int64_t E) {
     const double avg = static_cast<double>(R) / static_cast<double>(E);
     if (avg <= 4.0) return 16;
@@ -128,6 +132,9 @@ struct Layout {
     size_t flags = 0;
     int64_t n_flags = 0;
     size_t csum13 = 0, csum2 = 0;         // offset-code corrections (2-bit, 16-token tiles): [groups][R]
+    int light_max = 0;                    // 2-bit prefill plans: experts of at most this many rows get
+    int64_t max_light = 0;                //   a light tile list (8-row tiles) and launches of their own
+    size_t light_tiles = 0, n_light = 0;
     size_t total = 0;
 };
 
@@ -170,6 +177,14 @@ Layout make_layout(int64_t T, int64_t K, int64_t N, int64_t E, int topk, int bit
     const bool ga = bits == 2 && L.nt == 16;
     L.csum13 = o;   o = align_up(o + (ga ? sizeof(float) * L.R * (K / 128) : 0));
     L.csum2 = o;    o = align_up(o + (ga ? sizeof(float) * L.R * (N / 128) : 0));
+    // 2-bit batches routed by the large-batch kernels with 64- or 128-token
+    // tiles: experts with at most kLightRows rows (the skewed tail) are run by
+    // separate group-accumulate launches over 8-row tiles, whose work item
+    // costs about half of a full tile's for the same weights
+    L.light_max = (bits == 2 && L.nt >= 64 && L.R > kSmallRouteMax) ? kLightRows : 0;
+    L.max_light = L.light_max ? E : 0;   // one tile per light expert
+    L.light_tiles = o; o = align_up(o + sizeof(int4) * L.max_light);
+    L.n_light = o;     o = align_up(o + sizeof(int));
     L.total = o;
     return L;
 }
@@ -319,12 +334,13 @@ int check_workspace(const void* ws, size_t bytes, const Layout& L) {
 
 // Routing lists of the local experts [e_begin, e_begin + E) among E_total.
 int run_route(const int32_t* ids, int64_t E, const Layout& L, void* ws, cudaStream_t s, int64_t e_begin = 0,
-              int64_t E_total = -1) {
+              int64_t E_total = -1, int light_max = 0) {
     cudaError_t e = launch_route(ids, static_cast<int>(L.R), static_cast<int>(E), static_cast<int>(e_begin),
                                  static_cast<int>(E_total < 0 ? E : E_total), L.tile_rows, at<int>(ws, L.counts),
                                  at<int>(ws, L.offsets), at<int>(ws, L.perm), at<int>(ws, L.inv),
                                  at<int4>(ws, L.tiles), at<int>(ws, L.n_tiles), at<int>(ws, L.status),
-                                 at<int>(ws, L.chunks), s);
+                                 at<int>(ws, L.chunks), s, light_max, at<int4>(ws, L.light_tiles),
+                                 at<int>(ws, L.n_light));
     return e == cudaSuccess ? WNA16_OK : cuda_fail(e, "route kernel launch");
 }
 
@@ -342,16 +358,19 @@ struct GemmPlan {
 
 int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uint16_t* wscales, const void* b_src,
               void* out, int64_t K, int64_t N, int64_t E, int group, float limit, const Layout& L, void* ws,
-              int h_interleaved = 0, const float* csum = nullptr) {
+              int h_interleaved = 0, const float* csum = nullptr, bool light = false) {
     DevInfo dev;
     if (int rc = device_info(dev)) return rc;
     const int64_t kred = w13 ? K : N;
     const int64_t rows_per_expert = w13 ? 2 * N : K;
-    const int nt = L.nt;
+    // light: the light experts' launch, 16-token tiles (of at most 8 rows)
+    // over the light tile list, no K split (every output written directly)
+    const int nt = light ? 16 : L.nt;
     const int kp = stage_k(nt, bits, kred);
     const int pitch = kp * bits / 8;
-    const int64_t max_units = w13 ? L.units13 : L.units2;
-    const int ksplit = choose_split(max_units, kred, kp, group, nt, w13 ? 8 : 4);
+    const int64_t mt_units = w13 ? N / 128 : K / 256;
+    const int64_t max_units = light ? L.max_light * mt_units : (w13 ? L.units13 : L.units2);
+    const int ksplit = light ? 1 : choose_split(max_units, kred, kp, group, nt, w13 ? 8 : 4);
     const int ngroups = static_cast<int>(kred / group);
     GemmSmem sm = gemm_smem_layout(bits, nt, kp, ngroups / ksplit, dev.max_smem);
     if (sm.nstage < 2)
@@ -386,8 +405,8 @@ int plan_gemm(GemmPlan& P, bool w13, int bits, const int32_t* wpacked, const uin
     }
 
     GemmParams& gp = P.gp;
-    gp.tiles = at<const int4>(ws, L.tiles);
-    gp.n_tiles = at<const int>(ws, L.n_tiles);
+    gp.tiles = at<const int4>(ws, light ? L.light_tiles : L.tiles);
+    gp.n_tiles = at<const int>(ws, light ? L.n_light : L.n_tiles);
     gp.scales = wscales;
     gp.out = static_cast<__nv_bfloat16*>(out);
     gp.out_ld = static_cast<int>(w13 ? N : K);
@@ -581,6 +600,24 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
                            K, N, E, g2, swiglu_limit, L, workspace, false,
                            p13.gp.ksplit > 1 ? at<float>(workspace, L.csum2) : nullptr))
         return rc;
+    // Light experts of 2-bit prefill batches: two more launches, group-
+    // accumulate with plain codes over 8-row tiles and no K split, which write
+    // their rows of h and y themselves. The light w13 runs after the main w13's
+    // split-K finalize (which writes every row of h, the light ones from sums
+    // nobody parked) and overwrites those rows; the main w2 must write y
+    // itself (no split), since the combine reads every row of y. Kept only
+    // when both light plans fit and take the group-accumulate mode.
+    GemmPlan p13l, p2l;
+    int light_max = 0;
+    if (L.light_max > 0 && p2.gp.ksplit == 1) {
+        if (plan_gemm(p13l, true, bits, w13_packed, w13_scales, at<void>(workspace, L.xp), at<void>(workspace, L.h), K,
+                      N, E, group_size, swiglu_limit, L, workspace, il, nullptr, true) == WNA16_OK &&
+            plan_gemm(p2l, false, bits, w2_packed, w2_scales, at<void>(workspace, L.h), at<void>(workspace, L.y), K,
+                      N, E, g2, swiglu_limit, L, workspace, false, nullptr, true) == WNA16_OK &&
+            p13l.gp.ga && p2l.gp.ga)
+            light_max = L.light_max;
+        g_err[0] = 0;   // a light plan that does not fit only leaves the light path out
+    }
 
     mark(0, s);
     int launches = 0;
@@ -600,7 +637,7 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
         launches += 1;
         mark(1, s);
     } else {
-        if (int rc = run_route(topk_ids, E, L, workspace, s, e_begin, E_total)) return rc;
+        if (int rc = run_route(topk_ids, E, L, workspace, s, e_begin, E_total, light_max)) return rc;
         launches += route_chunks(static_cast<int>(L.R)) > 0 ? 3 : 1;
         mark(1, s);
         e = launch_gather(static_cast<const __nv_bfloat16*>(x), at<int>(workspace, L.inv), static_cast<int>(T), topk,
@@ -619,8 +656,12 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
                                 s);
         if (e != cudaSuccess) return cuda_fail(e, "finalize kernel launch");
     }
+    if (light_max)
+        if (int rc = launch_plan(p13l, s)) return rc;
     mark(3, s);
     if (int rc = launch_plan(p2, s)) return rc;
+    if (light_max)
+        if (int rc = launch_plan(p2l, s)) return rc;
     mark(4, s);
     if (p2.gp.ksplit > 1)      // split K: the combine adds the splits itself
         e = launch_combine_partials(at<float>(workspace, L.partial), p2.gp.ksplit, static_cast<int>(L.R), topk_weights,
@@ -633,7 +674,8 @@ int forward_impl(const void* x, const int32_t* topk_ids, const float* topk_weigh
     if (e != cudaSuccess) return cuda_fail(e, "combine kernel launch");
     mark(5, s);
     mark_done();
-    g_launches = launches + 3 + (p13.gp.ksplit > 1 && !p13.gp.fuse_splits ? 1 : 0);   // + w13 (+ finalize), w2, combine
+    // + w13 (+ finalize), w2, combine (+ the two light launches)
+    g_launches = launches + 3 + (p13.gp.ksplit > 1 && !p13.gp.fuse_splits ? 1 : 0) + (light_max ? 2 : 0);
     return WNA16_OK;
 }
 

@@ -77,9 +77,12 @@ cudaError_t ensure_dynamic_smem(const void* fn, int bytes);
 // route_chunks(R) * (E + 1) ints of chunk_scratch; smaller ones by one CTA.
 constexpr int kRouteChunkedMin = 8192;
 int route_chunks(int R);
+// With light_max > 0 (at most 8), experts of at most light_max rows get one
+// tile each in light_tiles (n_light of them) instead of the main list.
 cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int* counts,
                          int* offsets, int* perm, int* inv, int4* tiles, int* n_tiles, int* status,
-                         int* chunk_scratch, cudaStream_t stream);
+                         int* chunk_scratch, cudaStream_t stream, int light_max = 0, int4* light_tiles = nullptr,
+                         int* n_light = nullptr);
 // Routing lists and the gather of x rows in one kernel for small batches
 // (R <= kSmallRouteMax slots, E <= 1024): one CTA per slot.
 constexpr int kSmallRouteMax = 512;

@@ -78,10 +78,32 @@ __device__ __forceinline__ int local_expert(int g, int e_begin, int E, int E_tot
 // Also emits the token-tile list {expert, first row, rows} in expert order.
 // Only the experts [e_begin, e_begin + E) of the E_total are routed here
 // (all of them on a single device); slots of the other experts get inv = -1.
+// Light experts (at most light_max > 0 rows, and at most kLightTileRows: the
+// skewed tail of a prefill batch) leave the main tile list for a second one
+// with one tile per expert, run by launches of their own; both lists are in
+// expert order.
+constexpr int kLightTileRows = 8;
+__device__ __forceinline__ bool is_light(int c, int light_max) {
+    return light_max > 0 && c > 0 && c <= light_max && c <= kLightTileRows;
+}
+// Exclusive scan of the experts' light tile counts (the whole block calls it;
+// `scratch` is free again on return).
+__device__ __forceinline__ void light_scan(bool light, int c, int& loff, int& ltotal, int* scratch) {
+    __syncthreads();
+    int z0, z1;
+    block_exclusive_scan2(light ? (c + kLightTileRows - 1) / kLightTileRows : 0, 0, loff, z0, ltotal, z1, scratch);
+    __syncthreads();
+}
+__device__ __forceinline__ void write_light_tiles(int e, int c, int off, int4* dst) {
+    for (int j = 0; j * kLightTileRows < c; ++j)
+        dst[j] = make_int4(e, off + j * kLightTileRows, min(kLightTileRows, c - j * kLightTileRows), 0);
+}
+
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_kernel(const int32_t* __restrict__ ids, int R, int E, int e_begin, int E_total, int nt,
                  int* __restrict__ counts, int* __restrict__ offsets, int* __restrict__ perm, int* __restrict__ inv,
-                 int4* __restrict__ tiles, int* __restrict__ n_tiles, int* __restrict__ status) {
+                 int4* __restrict__ tiles, int* __restrict__ n_tiles, int* __restrict__ status, int light_max,
+                 int4* __restrict__ light_tiles, int* __restrict__ n_light) {
     extern __shared__ int sm[];
     int* cnt = sm;                          // [kRouteWarps][E]
     int* scratch = sm + kRouteWarps * E;    // 64 ints
@@ -120,18 +142,23 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
             c += v;
         }
     }
-    const int ntl = tid < E ? (c + nt - 1) / nt : 0;
+    const bool light = tid < E && is_light(c, light_max);
+    const int ntl = tid < E && !light ? (c + nt - 1) / nt : 0;
     int off, toff, total, ttotal;
     block_exclusive_scan2(c, ntl, off, toff, total, ttotal, scratch);
+    int loff = 0, ltotal = 0;
+    if (light_max > 0) light_scan(light, c, loff, ltotal, scratch);
     if (tid < E) {
         counts[tid] = c;
         offsets[tid] = off;
         for (int j = 0; j < ntl; ++j) tiles[toff + j] = make_int4(tid, off + j * nt, min(nt, c - j * nt), 0);
+        if (light) write_light_tiles(tid, c, off, light_tiles + loff);
         for (int w = 0; w < W; ++w) cnt[w * E + tid] += off;
     }
     if (tid == 0) {
         offsets[E] = total;
         *n_tiles = ttotal;
+        if (light_max > 0) *n_light = ltotal;
     }
     __syncthreads();
 
@@ -185,7 +212,8 @@ __global__ void __launch_bounds__(kChunkThreads)
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_scan_kernel(int nchunks, int E, int nt, int* __restrict__ ccount, const int* __restrict__ cbad,
                       int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ tiles,
-                      int* __restrict__ n_tiles, int* __restrict__ status) {
+                      int* __restrict__ n_tiles, int* __restrict__ status, int light_max,
+                      int4* __restrict__ light_tiles, int* __restrict__ n_light) {
     __shared__ int scratch[64];
     const int tid = threadIdx.x;
     if (tid == 0) {
@@ -208,13 +236,17 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
             for (int i = 0; i < kScanBatch; ++i) c_tot += v[i];
         }
     }
-    const int ntl = tid < E ? (c_tot + nt - 1) / nt : 0;
+    const bool light = tid < E && is_light(c_tot, light_max);
+    const int ntl = tid < E && !light ? (c_tot + nt - 1) / nt : 0;
     int off, toff, total, ttotal;
     block_exclusive_scan2(c_tot, ntl, off, toff, total, ttotal, scratch);
+    int loff = 0, ltotal = 0;
+    if (light_max > 0) light_scan(light, c_tot, loff, ltotal, scratch);
     if (tid < E) {
         counts[tid] = c_tot;
         offsets[tid] = off;
         for (int j = 0; j < ntl; ++j) tiles[toff + j] = make_int4(tid, off + j * nt, min(nt, c_tot - j * nt), 0);
+        if (light) write_light_tiles(tid, c_tot, off, light_tiles + loff);
         int run = off;
         for (int c0 = 0; c0 < nchunks; c0 += kScanBatch) {
             int v[kScanBatch];
@@ -231,6 +263,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     if (tid == 0) {
         offsets[E] = total;
         *n_tiles = ttotal;
+        if (light_max > 0) *n_light = ltotal;
     }
 }
 
@@ -853,7 +886,7 @@ int route_chunks(int R) { return R > kRouteChunkedMin ? (R + kChunk - 1) / kChun
 
 cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_total, int nt, int* counts, int* offsets,
                          int* perm, int* inv, int4* tiles, int* n_tiles, int* status, int* chunk_scratch,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, int light_max, int4* light_tiles, int* n_light) {
     const int nchunks = route_chunks(R);
     if (nchunks > 0) {
         int* ccount = chunk_scratch;                                  // [nchunks][E]
@@ -864,7 +897,7 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_to
         if (e != cudaSuccess) return e;
         route_count_kernel<<<nchunks, kChunkThreads, hsmem, stream>>>(ids, R, E, e_begin, E_total, ccount, cbad);
         route_scan_kernel<<<1, kRouteThreads, 0, stream>>>(nchunks, E, nt, ccount, cbad, counts, offsets, tiles,
-                                                          n_tiles, status);
+                                                          n_tiles, status, light_max, light_tiles, n_light);
         route_place_kernel<<<nchunks, kChunkThreads, psmem, stream>>>(ids, R, E, e_begin, E_total, ccount, perm, inv,
                                                                       status);
         return cudaGetLastError();
@@ -873,7 +906,7 @@ cudaError_t launch_route(const int32_t* ids, int R, int E, int e_begin, int E_to
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(route_kernel), smem);
     if (e != cudaSuccess) return e;
     route_kernel<<<1, kRouteThreads, smem, stream>>>(ids, R, E, e_begin, E_total, nt, counts, offsets, perm, inv,
-                                                    tiles, n_tiles, status);
+                                                    tiles, n_tiles, status, light_max, light_tiles, n_light);
     return cudaGetLastError();
 }
 
