@@ -295,11 +295,12 @@ WNA16_API int wna16_moe_profile(int slots);
 WNA16_API int wna16_moe_profile_read(float* ms, int n);
 
 /* Number of kernels the last successful wna16_moe_forward on the calling
- * thread launched (4 to 8 depending on the plan: routing in one kernel with
+ * thread launched (4 to 10 depending on the plan: routing in one kernel with
  * the gather for small batches, or in one or three kernels plus the gather;
  * w13, with a split-K finalize when decode-sized tiles split it (the two
  * splits of prefill-sized tiles are added inside the w13 kernel); w2;
- * combine); 0 before any. */
+ * combine; for 2-bit prefill batches with experts of at most 8 rows, one
+ * more w13 and one more w2 launch for those experts); 0 before any. */
 WNA16_API int wna16_moe_launches_last_forward(void);
 
 #ifdef __cplusplus
