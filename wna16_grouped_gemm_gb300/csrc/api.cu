@@ -60,11 +60,12 @@ int cuda_fail(cudaError_t e, const char* what) {
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 
-// Token tile (MMA N) from the mean rows per expert.
-constexpr int kLightRows = 8;   // light experts: at most this many rows (one 8-row tile; measured
-                                // 1.3 % faster on the 2-bit Zipf prefill than 16, whose 9-16-row
-                                // experts took two light tiles)
+// Light experts of 2-bit prefill batches: at most this many rows (one 8-row
+// tile; measured 1 % faster on the 2-bit Zipf prefill than 16, whose 9-16-row
+// experts took two light tiles).
+constexpr int kLightRows = 8;
 
+// Token tile (MMA N) from the mean rows per expert.
 int choose_nt(int64_t R, int64_t E) {
     const double avg = static_cast<double>(R) / static_cast<double>(E);
     if (avg <= 4.0) return 16;
