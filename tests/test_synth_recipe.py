@@ -10,13 +10,13 @@ import pytest
 import synth
 
 
-@pytest.mark.parametrize("name,active,max_rows,min_rows,top5", [
-    ("decode_w2", 29, 2, 1, [2, 2, 2, 1, 1]),
-    ("decode_w4_T1", 8, 1, 1, [1, 1, 1, 1, 1]),
-    ("prefill_w2_zipf", 142, 1990, 1, [1990, 1788, 1538, 1285, 1176]),
-    ("prefill_w4_g64", 256, 296, 210, [296, 295, 295, 294, 291]),
+@pytest.mark.parametrize("name,active,max_rows,min_rows,top5,light", [
+    ("decode_w2", 29, 2, 1, [2, 2, 2, 1, 1], (29, 32)),
+    ("decode_w4_T1", 8, 1, 1, [1, 1, 1, 1, 1], (8, 8)),
+    ("prefill_w2_zipf", 142, 1990, 1, [1990, 1788, 1538, 1285, 1176], (80, 210)),
+    ("prefill_w4_g64", 256, 296, 210, [296, 295, 295, 294, 291], (0, 0)),
 ])
-def test_routing_statistics(name, active, max_rows, min_rows, top5):
+def test_routing_statistics(name, active, max_rows, min_rows, top5, light):
     w = synth.get(name)
     ids, weights = synth.make_routing(w, 0)
     assert ids.shape == (w.T, w.topk) and ids.dtype == np.int32
@@ -26,6 +26,10 @@ def test_routing_statistics(name, active, max_rows, min_rows, top5):
     assert int(counts.max()) == max_rows
     assert int(counts[counts > 0].min()) == min_rows
     assert sorted(counts.tolist(), reverse=True)[:5] == top5
+    # experts of at most 8 rows (the light-expert launches of 2-bit prefill
+    # batches): how many, and their rows
+    few = (counts > 0) & (counts <= 8)
+    assert (int(few.sum()), int(counts[few].sum())) == light
     # top-k: distinct experts per token, weights renormalised, descending
     assert all(len(set(r)) == w.topk for r in ids.tolist())
     assert np.allclose(weights.sum(axis=1), 1.0, atol=1e-6)
